@@ -1,0 +1,192 @@
+"""gemm_gather for GB300: tiled all-gather over a symmetric heap, alone and
+fused into the epilogue of a matmul (iris PR #626, iris #594, iris #591).
+
+Thin Python binding of the C ABI in include/gemm_gather.h (same names, minus
+the ``gg_`` prefix).  It only marshals arguments: torch tensors become device
+pointers, the current torch stream becomes the launch stream.  Every step of
+the data path runs in the library's CUDA kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from ._lib import (GG_AG_AUTO, GG_AG_BULK, GG_AG_VECTOR, GG_BF16, GG_ERR_ALIGNMENT,
+                   GG_ERR_CUDA, GG_ERR_INVALID_ARG, GG_ERR_NOT_IN_HEAP, GG_ERR_TIMEOUT,
+                   GG_ERR_UNSUPPORTED, GG_F16, GG_F32, GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N,
+                   GG_MAX_WORLD, GG_OK, GGError, Group, Tile, check, lib, LIB_PATH)
+
+__all__ = [
+    "heap_create", "heap_wrap", "heap_bases", "heap_info", "heap_destroy", "all_gather",
+    "all_gather_check", "matmul_all_gather", "matmul_all_gather_check", "set_wait_limit_ns",
+    "get_wait_limit_ns", "SymmetricHeap", "Heap", "GGError", "DTYPE_CODES", "PATHS",
+    "FUSED_TILE",
+]
+
+DTYPE_CODES = {torch.float16: GG_F16, torch.bfloat16: GG_BF16, torch.float32: GG_F32}
+PATHS = {"auto": GG_AG_AUTO, "bulk": GG_AG_BULK, "vector": GG_AG_VECTOR}
+FUSED_TILE = (GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N)
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        if torch.cuda.is_available() and torch.cuda.is_initialized():
+            return torch.cuda.current_stream().cuda_stream or None
+        return None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream or None
+    return int(stream) or None
+
+
+def _dtype(d) -> int:
+    if isinstance(d, torch.dtype):
+        return DTYPE_CODES[d]
+    return {"f16": GG_F16, "bf16": GG_BF16, "f32": GG_F32}.get(d, d)
+
+
+@dataclass
+class Heap:
+    """Host handle of a symmetric heap (wraps ``gg_heap*``)."""
+    handle: int
+
+    def __del__(self):
+        if getattr(self, "handle", None):
+            lib.gg_heap_destroy(self.handle)
+            self.handle = None
+
+
+# --------------------------------------------------------------------------- #
+# C ABI, one function per entry point                                         #
+# --------------------------------------------------------------------------- #
+
+def heap_create(dev_base, bytes_per_rank: int, num_heaps: int, dev_bases_table,
+                stream=None) -> Heap:
+    out = ctypes.c_void_p()
+    check(lib.gg_heap_create(_ptr(dev_base), bytes_per_rank, num_heaps, _ptr(dev_bases_table),
+                             _stream(stream), ctypes.byref(out)))
+    return Heap(out.value)
+
+
+def heap_wrap(dev_base, bytes_per_rank: int, num_heaps: int, dev_bases_table) -> Heap:
+    out = ctypes.c_void_p()
+    check(lib.gg_heap_wrap(_ptr(dev_base), bytes_per_rank, num_heaps, _ptr(dev_bases_table),
+                           ctypes.byref(out)))
+    return Heap(out.value)
+
+
+def heap_bases(heap: Heap, n: int | None = None) -> list[int]:
+    if n is None:
+        n = heap_info(heap)[0]
+    buf = (ctypes.c_uint64 * n)()
+    check(lib.gg_heap_bases(heap.handle, buf, n))
+    return list(buf)
+
+
+def heap_info(heap: Heap) -> tuple[int, int]:
+    h, part = ctypes.c_int(), ctypes.c_size_t()
+    check(lib.gg_heap_info(heap.handle, ctypes.byref(h), ctypes.byref(part)))
+    return h.value, part.value
+
+
+def heap_destroy(heap: Heap) -> None:
+    if heap.handle:
+        check(lib.gg_heap_destroy(heap.handle))
+        heap.handle = None
+
+
+def all_gather(heap: Heap, rank: int, input, ld_in: int, output, ld_out: int, M: int, N: int,
+               dtype, tile: tuple[int, int], comm_programs: int,
+               group: tuple[int, int, int], status=None, stream=None, path: str = "auto") -> None:
+    check(lib.gg_all_gather_path(heap.handle, rank, _ptr(input), ld_in, _ptr(output), ld_out, M,
+                                 N, _dtype(dtype), Tile(*tile), comm_programs, Group(*group),
+                                 _ptr(status), _stream(stream), PATHS[path]))
+
+
+def all_gather_check(heap: Heap, rank: int, input, ld_in: int, output, ld_out: int, M: int,
+                     N: int, dtype, tile: tuple[int, int], comm_programs: int,
+                     group: tuple[int, int, int], path: str = "auto") -> str:
+    """Validate without launching; returns the path a launch would take."""
+    chosen = ctypes.c_int()
+    check(lib.gg_all_gather_check(heap.handle, rank, _ptr(input), ld_in, _ptr(output), ld_out, M,
+                                  N, _dtype(dtype), Tile(*tile), comm_programs, Group(*group),
+                                  PATHS[path], ctypes.byref(chosen)))
+    return {GG_AG_AUTO: "none", GG_AG_BULK: "bulk", GG_AG_VECTOR: "vector"}[chosen.value]
+
+
+def matmul_all_gather(heap: Heap, rank: int, A, lda: int, B, ldb: int, output, ld_out: int,
+                      M: int, N: int, K: int, dtype, tile: tuple[int, int], comm_programs: int,
+                      group: tuple[int, int, int], status=None, stream=None) -> None:
+    check(lib.gg_matmul_all_gather(heap.handle, rank, _ptr(A), lda, _ptr(B), ldb, _ptr(output),
+                                   ld_out, M, N, K, _dtype(dtype), Tile(*tile), comm_programs,
+                                   Group(*group), _ptr(status), _stream(stream)))
+
+
+def matmul_all_gather_check(heap: Heap, rank: int, A, lda: int, B, ldb: int, output,
+                            ld_out: int, M: int, N: int, K: int, dtype, tile: tuple[int, int],
+                            comm_programs: int, group: tuple[int, int, int]) -> None:
+    check(lib.gg_matmul_all_gather_check(heap.handle, rank, _ptr(A), lda, _ptr(B), ldb,
+                                         _ptr(output), ld_out, M, N, K, _dtype(dtype),
+                                         Tile(*tile), comm_programs, Group(*group)))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    check(lib.gg_set_wait_limit_ns(ns))
+
+
+def get_wait_limit_ns() -> int:
+    return int(lib.gg_get_wait_limit_ns())
+
+
+# --------------------------------------------------------------------------- #
+# Device memory for a heap (torch allocates; the library never does)          #
+# --------------------------------------------------------------------------- #
+
+class SymmetricHeap:
+    """H partitions of ``part_bytes`` each in one torch device allocation,
+    plus the device heap-bases table, registered with ``gg_heap_create``."""
+
+    ALIGN = 256
+
+    def __init__(self, num_heaps: int, part_bytes: int, device="cuda", fill: int | None = None,
+                 stream=None):
+        if part_bytes % self.ALIGN:
+            part_bytes += self.ALIGN - part_bytes % self.ALIGN
+        self.H = num_heaps
+        self.part_bytes = part_bytes
+        raw = torch.empty(num_heaps * part_bytes + self.ALIGN, dtype=torch.uint8, device=device)
+        shift = (-raw.data_ptr()) % self.ALIGN
+        self._raw = raw
+        self.storage = raw[shift: shift + num_heaps * part_bytes]
+        if fill is not None:
+            self.storage.fill_(fill)
+        self.table = torch.empty(num_heaps, dtype=torch.int64, device=device)
+        self.heap = heap_create(self.storage, part_bytes, num_heaps, self.table, stream=stream)
+
+    @property
+    def base(self) -> int:
+        return self.storage.data_ptr()
+
+    def partition(self, h: int) -> torch.Tensor:
+        return self.storage[h * self.part_bytes: (h + 1) * self.part_bytes]
+
+    def view(self, h: int, offset: int, rows: int, cols: int, ld: int,
+             dtype: torch.dtype) -> torch.Tensor:
+        """rows x cols view (row pitch ld elements) at ``offset`` in partition h."""
+        es = torch.empty((), dtype=dtype).element_size()
+        assert offset % es == 0
+        n = ((rows - 1) * ld + cols) if rows else 0
+        flat = self.partition(h)[offset: offset + n * es].view(dtype)
+        return flat.as_strided((rows, cols), (ld, 1))
+
+    def ptr(self, h: int, offset: int) -> int:
+        return self.base + h * self.part_bytes + offset

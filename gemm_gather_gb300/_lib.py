@@ -1,0 +1,103 @@
+"""ctypes loader of libgemm_gather.so (built in-tree by gemm_gather_gb300.build).
+
+Importing this module fails loudly when the library has not been built: there
+is no fallback path of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libgemm_gather.so")
+
+GG_OK = 0
+GG_ERR_INVALID_ARG = -1
+GG_ERR_ALIGNMENT = -2
+GG_ERR_NOT_IN_HEAP = -3
+GG_ERR_UNSUPPORTED = -4
+GG_ERR_CUDA = -5
+GG_ERR_TIMEOUT = -6
+
+GG_F16, GG_BF16, GG_F32 = 0, 1, 2
+GG_AG_AUTO, GG_AG_BULK, GG_AG_VECTOR = 0, 1, 2
+GG_MAX_WORLD = 64
+GG_MAX_HEAPS = 1024
+GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N = 128, 256
+
+# Every entry point declared in include/gemm_gather.h.
+EXPORTS = (
+    "gg_heap_create", "gg_heap_wrap", "gg_heap_bases", "gg_heap_info", "gg_heap_destroy",
+    "gg_all_gather", "gg_all_gather_path", "gg_all_gather_check",
+    "gg_matmul_all_gather", "gg_matmul_all_gather_check",
+    "gg_set_wait_limit_ns", "gg_get_wait_limit_ns",
+    "gg_last_error", "gg_status_string", "gg_version",
+)
+
+
+class Tile(ctypes.Structure):
+    _fields_ = [("block_m", ctypes.c_int), ("block_n", ctypes.c_int)]
+
+
+class Group(ctypes.Structure):
+    _fields_ = [("rank_start", ctypes.c_int), ("rank_stride", ctypes.c_int),
+                ("world_size", ctypes.c_int)]
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    vp, i32, i64, u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64
+    sz = ctypes.c_size_t
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    sig = {
+        "gg_heap_create": ([vp, sz, i32, vp, vp, pp], i32),
+        "gg_heap_wrap": ([vp, sz, i32, vp, pp], i32),
+        "gg_heap_bases": ([vp, ctypes.POINTER(u64), i32], i32),
+        "gg_heap_info": ([vp, ctypes.POINTER(i32), ctypes.POINTER(sz)], i32),
+        "gg_heap_destroy": ([vp], i32),
+        "gg_all_gather": ([vp, i32, vp, i64, vp, i64, i64, i64, i32, Tile, i32, Group, vp, vp],
+                          i32),
+        "gg_all_gather_path": ([vp, i32, vp, i64, vp, i64, i64, i64, i32, Tile, i32, Group, vp,
+                                vp, i32], i32),
+        "gg_all_gather_check": ([vp, i32, vp, i64, vp, i64, i64, i64, i32, Tile, i32, Group, i32,
+                                 ctypes.POINTER(i32)], i32),
+        "gg_matmul_all_gather": ([vp, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, i32, Tile,
+                                  i32, Group, vp, vp], i32),
+        "gg_matmul_all_gather_check": ([vp, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, i32,
+                                        Tile, i32, Group], i32),
+        "gg_set_wait_limit_ns": ([u64], i32),
+        "gg_get_wait_limit_ns": ([], u64),
+        "gg_last_error": ([], ctypes.c_char_p),
+        "gg_status_string": ([i32], ctypes.c_char_p),
+        "gg_version": ([], i32),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
+
+
+def load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()' or "
+            "python gemm_gather_gb300/build.py)")
+    return _declare(ctypes.CDLL(LIB_PATH))
+
+
+lib = load()
+
+
+class GGError(RuntimeError):
+    """A gemm_gather call returned a status other than GG_OK."""
+
+    def __init__(self, status: int, message: str):
+        self.status = status
+        name = lib.gg_status_string(status).decode()
+        super().__init__(f"{name}: {message}")
+
+
+def check(status: int) -> None:
+    if status != GG_OK:
+        raise GGError(status, lib.gg_last_error().decode())

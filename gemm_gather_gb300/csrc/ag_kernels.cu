@@ -1,0 +1,301 @@
+// Persistent tiled all-gather over a symmetric heap (sm_103a).
+//
+// What it computes (iris #594 "Multi-GPU CI", iris PR #626 "Summary"):
+// every source block (one group member's M x N input) is written into its row
+// block of the gathered output of every group member.  How (iris PR #626
+// "Summary" and "Triton CCL all-gather"; iris #591 Description §1):
+//  * the heap-bases table is read once per program, before the tile loop, and
+//    turned into one output base per member (the hoisted per-peer translation;
+//    no base is reloaded inside the loop);
+//  * each tile is read from HBM once and staged on chip;
+//  * the staged tile is stored to the local copy first, then to the peers in
+//    rotated order (i+1, i+2, ... mod W), with no fence or reload between
+//    destinations.
+//
+// Two data paths with identical results:
+//  * bulk:   tiles are staged in shared memory by the TMA engine
+//            (cp.async.bulk, completion on an mbarrier) and stored with
+//            cp.async.bulk shared->global, one copy per tile row and
+//            destination.  Four warps per program run independent pipelines
+//            over a ring of stages; a stage is refilled once the stores that
+//            read it have finished reading shared memory.
+//  * vector: 16/8/4/2-byte loads into registers, then one store per
+//            destination; several tiles' loads are in flight per thread.
+#include <cuda_runtime.h>
+
+#include "gg_internal.h"
+#include "ptx.cuh"
+
+namespace gg {
+namespace {
+
+constexpr int kAgWarps = 4;           // most independent pipelines (warps) per program
+constexpr int kAgMaxStages = 16;      // ring stages per pipeline
+constexpr int kAgSmemBudget = 192 * 1024;
+constexpr uint64_t kDrainLimitNs = 1000000000ull;  // waits for copies already in flight
+
+struct AgShared {
+    uint64_t full[kAgWarps][kAgMaxStages];  // one mbarrier per ring stage
+    uint64_t dst[kMaxWorld];                // output base of member i
+    uint64_t src[kMaxWorld];                // input base of member i
+};
+
+constexpr int kAgHeader = (int)((sizeof(AgShared) + 127) / 128 * 128);
+
+struct Item {
+    int g;          // group index of the source
+    int64_t tm, tn; // tile coordinates
+    int rows;       // valid rows of the tile
+    uint32_t rb;    // valid bytes per tile row
+};
+
+__device__ __forceinline__ Item decode_item(const GatherArgs &a, int64_t t)
+{
+    Item it;
+    const int64_t s = t / a.tiles_per_src;
+    const int64_t tile = t - s * a.tiles_per_src;
+    it.g = a.src_first + (int)s;
+    it.tm = tile / a.tiles_n;
+    it.tn = tile - it.tm * a.tiles_n;
+    const int64_t r0 = it.tm * a.bm;
+    it.rows = (int)gg_min64(a.bm, a.M - r0);
+    const int64_t c0 = it.tn * a.bn_b;
+    it.rb = (uint32_t)gg_min64(a.bn_b, a.row_b - c0);
+    return it;
+}
+
+// Heap bases -> per-member input and output bases, once per program.
+__device__ __forceinline__ void load_member_bases(const GatherArgs &a, uint64_t *dst,
+                                                  uint64_t *src)
+{
+    for (int i = threadIdx.x; i < a.W; i += blockDim.x) {
+        const uint64_t base = a.bases[a.rank_start + i * a.rank_stride];
+        dst[i] = base + (uint64_t)a.out_off;
+        src[i] = a.in_abs ? reinterpret_cast<uint64_t>(a.in_abs) : base + (uint64_t)a.in_off;
+    }
+}
+
+// D: store groups a pipeline may leave reading shared memory before it
+// refills the oldest stage; the loads run stages - D items ahead.
+template <int D>
+__global__ void __launch_bounds__(kAgWarps * 32)
+    ag_bulk_kernel(const GatherArgs a, int stages, int stage_bytes)
+{
+    const int npipe = blockDim.x >> 5;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    AgShared &sh = *reinterpret_cast<AgShared *>(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    load_member_bases(a, sh.dst, sh.src);
+    if (threadIdx.x == 0) {
+        for (int w = 0; w < npipe; ++w)
+            for (int s = 0; s < stages; ++s)
+                ptx::mbar_init(ptx::smem_addr(&sh.full[w][s]), 1);
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+
+    // Items of this pipeline: blockIdx.x + (warp + npipe*k) * gridDim.x.
+    const int64_t step = (int64_t)gridDim.x * npipe;
+    const int64_t first = blockIdx.x + (int64_t)warp * gridDim.x;
+    const int64_t n_local = first < a.total_items ? (a.total_items - 1 - first) / step + 1 : 0;
+    const int lookahead = stages - D;  // loads in flight ahead of the stores
+
+    const uint32_t ring = ptx::smem_addr(smem + kAgHeader) + (uint32_t)(warp * stages * stage_bytes);
+    const uint32_t full0 = ptx::smem_addr(&sh.full[warp][0]);
+    const uint32_t pitch = (uint32_t)a.bn_b;  // staged row pitch (multiple of 16)
+
+    auto issue_load = [&](int64_t k) {
+        const Item it = decode_item(a, first + k * step);
+        const int st = (int)(k % stages);
+        const uint32_t bar = full0 + 8u * st;
+        const uint32_t buf = ring + (uint32_t)st * stage_bytes;
+        if (lane == 0)
+            ptx::mbar_arrive_expect_tx(bar, (uint32_t)it.rows * it.rb);
+        __syncwarp();
+        const uint8_t *src = reinterpret_cast<const uint8_t *>(sh.src[it.g]) +
+                             it.tm * a.bm * a.ld_in_b + it.tn * a.bn_b;
+        for (int r = lane; r < it.rows; r += 32)
+            ptx::bulk_g2s(buf + (uint32_t)r * pitch, src + r * a.ld_in_b, it.rb, bar);
+    };
+
+    const int64_t preload = gg_min64(lookahead, n_local);
+    for (int64_t k = 0; k < preload; ++k)
+        issue_load(k);
+
+    int64_t k = 0;
+    bool ok = true;
+    for (; k < n_local; ++k) {
+        const int st = (int)(k % stages);
+        const uint32_t parity = (uint32_t)((k / stages) & 1);
+        const bool mine = ptx::mbar_wait(full0 + 8u * st, parity, a.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, mine)) {
+            ok = false;
+            break;
+        }
+        const Item it = decode_item(a, first + k * step);
+        const uint32_t buf = ring + (uint32_t)st * stage_bytes;
+        const int64_t row0 = (int64_t)it.g * a.M + it.tm * a.bm;
+        const int64_t col0 = it.tn * a.bn_b;
+        const int pairs = it.rows * a.W;
+        // pair p -> destination j = p / rows (j = 0 is the local copy), row p % rows
+        for (int p = lane; p < pairs; p += 32) {
+            const int j = p / it.rows;
+            const int r = p - j * it.rows;
+            int i = it.g + j;
+            if (i >= a.W)
+                i -= a.W;
+            uint8_t *dst = reinterpret_cast<uint8_t *>(sh.dst[i]) + (row0 + r) * a.ld_out_b + col0;
+            ptx::bulk_s2g(dst, buf + (uint32_t)r * pitch, it.rb);
+        }
+        ptx::bulk_commit();
+        const int64_t kk = k + lookahead;
+        if (kk < n_local) {
+            if (kk >= stages) {
+                // the stage of item kk last held item kk - stages = k - D
+                ptx::bulk_wait_read<D>();
+                __syncwarp();
+            }
+            issue_load(kk);
+        }
+    }
+
+    if (!ok) {
+        report_status(a.status, kStatusTimeout);
+        // loads issued but not consumed: items k .. min(k + lookahead, n_local) - 1
+        const int64_t end = gg_min64(k + lookahead, n_local);
+        for (int64_t q = k; q < end; ++q) {
+            const int st = (int)(q % stages);
+            ptx::mbar_wait(full0 + 8u * st, (uint32_t)((q / stages) & 1), kDrainLimitNs);
+        }
+    }
+    ptx::bulk_wait_all();
+}
+
+template <int VB>
+struct VecType;
+template <>
+struct VecType<16> { using T = uint4; };
+template <>
+struct VecType<8> { using T = uint2; };
+template <>
+struct VecType<4> { using T = uint32_t; };
+template <>
+struct VecType<2> { using T = uint16_t; };
+
+constexpr int kVecThreads = 512;
+constexpr int kVecUnroll = 4;
+
+template <int VB>
+__global__ void __launch_bounds__(kVecThreads) ag_vec_kernel(const GatherArgs a)
+{
+    using V = typename VecType<VB>::T;
+    __shared__ uint64_t dst[kMaxWorld];
+    __shared__ uint64_t src[kMaxWorld];
+    load_member_bases(a, dst, src);
+    __syncthreads();
+
+    const int crow = (int)(a.bn_b / VB);           // vectors per full tile row
+    const int tile_vecs = a.bm * crow;             // vectors per full tile
+    const int64_t stride = (int64_t)gridDim.x * kVecUnroll;
+
+    for (int64_t base = blockIdx.x; base < a.total_items; base += stride) {
+        for (int c = threadIdx.x; c < tile_vecs; c += blockDim.x) {
+            const int r = c / crow;
+            const int cc = c - r * crow;
+            V v[kVecUnroll];
+            bool valid[kVecUnroll];
+            Item it[kVecUnroll];
+#pragma unroll
+            for (int u = 0; u < kVecUnroll; ++u) {
+                const int64_t t = base + (int64_t)u * gridDim.x;
+                valid[u] = false;
+                if (t < a.total_items) {
+                    it[u] = decode_item(a, t);
+                    valid[u] = r < it[u].rows && (uint32_t)cc * VB < it[u].rb;
+                    if (valid[u]) {
+                        const uint8_t *s = reinterpret_cast<const uint8_t *>(src[it[u].g]) +
+                                           (it[u].tm * a.bm + r) * a.ld_in_b + it[u].tn * a.bn_b +
+                                           (int64_t)cc * VB;
+                        v[u] = *reinterpret_cast<const V *>(s);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kVecUnroll; ++u) {
+                if (!valid[u])
+                    continue;
+                const int64_t off = ((int64_t)it[u].g * a.M + it[u].tm * a.bm + r) * a.ld_out_b +
+                                    it[u].tn * a.bn_b + (int64_t)cc * VB;
+                for (int j = 0; j < a.W; ++j) {
+                    int i = it[u].g + j;
+                    if (i >= a.W)
+                        i -= a.W;
+                    *reinterpret_cast<V *>(reinterpret_cast<uint8_t *>(dst[i]) + off) = v[u];
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+// Ring geometry of the bulk path for a tile of `stage_raw` bytes: pipelines
+// per program, stages per pipeline and read depth D.  False if it cannot fit.
+bool bulk_geometry(int64_t stage_raw, int *npipe, int *stages, int *depth, int *stage_bytes)
+{
+    const int64_t sb = (stage_raw + 1023) / 1024 * 1024;
+    for (int np = kAgWarps; np >= 1; np >>= 1) {
+        const int64_t st = gg_min64(kAgMaxStages, (kAgSmemBudget - kAgHeader) / (np * sb));
+        if (st >= 6) {
+            *npipe = np; *stages = (int)st; *depth = 4; *stage_bytes = (int)sb;
+            return true;
+        }
+    }
+    const int64_t st = gg_min64(kAgMaxStages, (kAgSmemBudget - kAgHeader) / sb);
+    if (st >= 3) {
+        *npipe = 1; *stages = (int)st; *depth = st >= 4 ? 2 : 1; *stage_bytes = (int)sb;
+        return true;
+    }
+    return false;
+}
+
+template <int D>
+static cudaError_t launch_bulk_depth(const GatherArgs &a, int programs, int npipe, int stages,
+                                     int stage_bytes, cudaStream_t s)
+{
+    const int smem = kAgHeader + npipe * stages * stage_bytes;
+    cudaError_t e =
+        cudaFuncSetAttribute(ag_bulk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess)
+        return e;
+    ag_bulk_kernel<D><<<programs, npipe * 32, smem, s>>>(a, stages, stage_bytes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_bulk(const GatherArgs &a, int programs, cudaStream_t s)
+{
+    int npipe, stages, depth, stage_bytes;
+    if (!bulk_geometry((int64_t)a.bm * a.bn_b, &npipe, &stages, &depth, &stage_bytes))
+        return cudaErrorInvalidValue;  // tile too large (the host validates first)
+    switch (depth) {
+    case 4: return launch_bulk_depth<4>(a, programs, npipe, stages, stage_bytes, s);
+    case 2: return launch_bulk_depth<2>(a, programs, npipe, stages, stage_bytes, s);
+    default: return launch_bulk_depth<1>(a, programs, npipe, stages, stage_bytes, s);
+    }
+}
+
+cudaError_t launch_gather_vec(const GatherArgs &a, int programs, int vec_bytes, cudaStream_t s)
+{
+    switch (vec_bytes) {
+    case 16: ag_vec_kernel<16><<<programs, kVecThreads, 0, s>>>(a); break;
+    case 8: ag_vec_kernel<8><<<programs, kVecThreads, 0, s>>>(a); break;
+    case 4: ag_vec_kernel<4><<<programs, kVecThreads, 0, s>>>(a); break;
+    case 2: ag_vec_kernel<2><<<programs, kVecThreads, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gg

@@ -1,0 +1,521 @@
+// C ABI of gemm_gather: heap handles, argument validation, path selection and
+// launches.  Declared in include/gemm_gather.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+#include <vector>
+
+#include "../../include/gemm_gather.h"
+#include "gg_internal.h"
+
+struct gg_heap {
+    uint64_t base;
+    size_t part;
+    int H;
+    uint64_t *dev_table;
+    std::vector<uint64_t> host_bases;
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+
+gg_status fail(gg_status s, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+gg_status ok()
+{
+    g_last_error.clear();
+    return GG_OK;
+}
+
+gg_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(GG_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+int elem_size(gg_dtype d)
+{
+    switch (d) {
+    case GG_F16: return 2;
+    case GG_BF16: return 2;
+    case GG_F32: return 4;
+    }
+    return 0;
+}
+
+// Group checks shared by every collective; on success *gi is the group index
+// of `rank` (or -1 for a launch over all members).
+gg_status check_group(const gg_heap *heap, gg_group g, int rank, int *gi)
+{
+    if (!heap)
+        return fail(GG_ERR_INVALID_ARG, "heap is NULL");
+    if (g.world_size < 1 || g.world_size > GG_MAX_WORLD)
+        return fail(GG_ERR_INVALID_ARG, "world_size %d outside [1, %d]", g.world_size,
+                    GG_MAX_WORLD);
+    if (g.rank_stride < 1)
+        return fail(GG_ERR_INVALID_ARG, "rank_stride %d must be >= 1", g.rank_stride);
+    if (g.rank_start < 0)
+        return fail(GG_ERR_INVALID_ARG, "rank_start %d must be >= 0", g.rank_start);
+    const int64_t last = (int64_t)g.rank_start + (int64_t)(g.world_size - 1) * g.rank_stride;
+    if (last >= heap->H)
+        return fail(GG_ERR_INVALID_ARG, "group member %lld is not a heap (heaps: %d)",
+                    (long long)last, heap->H);
+    if (rank == -1) {
+        *gi = -1;
+        return GG_OK;
+    }
+    if (rank < 0 || rank >= heap->H)
+        return fail(GG_ERR_INVALID_ARG, "rank %d is neither -1 nor a heap index", rank);
+    const int d = rank - g.rank_start;
+    if (d < 0 || d % g.rank_stride != 0 || d / g.rank_stride >= g.world_size)
+        return fail(GG_ERR_INVALID_ARG, "rank %d is not a member of the group (%d, %d, %d)", rank,
+                    g.rank_start, g.rank_stride, g.world_size);
+    *gi = d / g.rank_stride;
+    return GG_OK;
+}
+
+// Byte offset of a symmetric buffer within its partition, checking that
+// `extent` bytes from there stay inside the partition.
+gg_status symmetric_offset(const gg_heap *heap, const void *p, int64_t extent, const char *what,
+                           int64_t *off)
+{
+    const uint64_t a = reinterpret_cast<uint64_t>(p);
+    const uint64_t end = heap->base + (uint64_t)heap->part * (uint64_t)heap->H;
+    if (a < heap->base || a >= end)
+        return fail(GG_ERR_NOT_IN_HEAP, "%s (0x%llx) is not inside the heap", what,
+                    (unsigned long long)a);
+    const uint64_t o = (a - heap->base) % heap->part;
+    if ((uint64_t)extent > heap->part - o)
+        return fail(GG_ERR_NOT_IN_HEAP,
+                    "%s: %lld bytes at offset %llu overrun the %llu-byte partition", what,
+                    (long long)extent, (unsigned long long)o, (unsigned long long)heap->part);
+    *off = (int64_t)o;
+    return GG_OK;
+}
+
+bool overlap(uint64_t a0, uint64_t a1, uint64_t b0, uint64_t b1) { return a0 < b1 && b0 < a1; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool checked_mul(int64_t a, int64_t b, int64_t *out)
+{
+    if (a != 0 && b > INT64_MAX / a)
+        return false;
+    *out = a * b;
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+gg_status gg_heap_wrap(void *dev_base, size_t bytes_per_rank, int num_heaps,
+                       uint64_t *dev_bases_table, gg_heap **out)
+{
+    if (!out)
+        return fail(GG_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!dev_base || !dev_bases_table)
+        return fail(GG_ERR_INVALID_ARG, "dev_base and dev_bases_table must be non-NULL");
+    if (reinterpret_cast<uint64_t>(dev_base) % 256 != 0)
+        return fail(GG_ERR_ALIGNMENT, "dev_base must be 256-byte aligned");
+    if (reinterpret_cast<uint64_t>(dev_bases_table) % 8 != 0)
+        return fail(GG_ERR_ALIGNMENT, "dev_bases_table must be 8-byte aligned");
+    if (bytes_per_rank == 0 || bytes_per_rank % 256 != 0)
+        return fail(GG_ERR_INVALID_ARG, "bytes_per_rank must be a positive multiple of 256");
+    if (num_heaps < 1 || num_heaps > GG_MAX_HEAPS)
+        return fail(GG_ERR_INVALID_ARG, "num_heaps %d outside [1, %d]", num_heaps, GG_MAX_HEAPS);
+    gg_heap *h = new gg_heap;
+    h->base = reinterpret_cast<uint64_t>(dev_base);
+    h->part = bytes_per_rank;
+    h->H = num_heaps;
+    h->dev_table = dev_bases_table;
+    h->host_bases.resize(num_heaps);
+    for (int i = 0; i < num_heaps; ++i)
+        h->host_bases[i] = h->base + (uint64_t)i * bytes_per_rank;
+    *out = h;
+    return ok();
+}
+
+gg_status gg_heap_create(void *dev_base, size_t bytes_per_rank, int num_heaps,
+                         uint64_t *dev_bases_table, gg_stream_t stream, gg_heap **out)
+{
+    gg_status st = gg_heap_wrap(dev_base, bytes_per_rank, num_heaps, dev_bases_table, out);
+    if (st != GG_OK)
+        return st;
+    gg_heap *h = *out;
+    cudaError_t e = cudaMemcpyAsync(dev_bases_table, h->host_bases.data(),
+                                    sizeof(uint64_t) * num_heaps, cudaMemcpyHostToDevice,
+                                    reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        delete h;
+        *out = nullptr;
+        return cuda_fail(e, "writing the heap-bases table");
+    }
+    return ok();
+}
+
+gg_status gg_heap_bases(const gg_heap *heap, uint64_t *host_out, int n)
+{
+    if (!heap || !host_out)
+        return fail(GG_ERR_INVALID_ARG, "heap and host_out must be non-NULL");
+    if (n < 0 || n > heap->H)
+        return fail(GG_ERR_INVALID_ARG, "n %d outside [0, %d]", n, heap->H);
+    std::copy(heap->host_bases.begin(), heap->host_bases.begin() + n, host_out);
+    return ok();
+}
+
+gg_status gg_heap_info(const gg_heap *heap, int *num_heaps, size_t *bytes_per_rank)
+{
+    if (!heap)
+        return fail(GG_ERR_INVALID_ARG, "heap is NULL");
+    if (num_heaps)
+        *num_heaps = heap->H;
+    if (bytes_per_rank)
+        *bytes_per_rank = heap->part;
+    return ok();
+}
+
+gg_status gg_heap_destroy(gg_heap *heap)
+{
+    delete heap;
+    return ok();
+}
+
+}  // extern "C"
+
+namespace {
+
+// Validation and argument set-up of a gather; *launch is false when there is
+// nothing to do (M == 0 or N == 0).
+gg_status prepare_gather(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
+                         void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
+                         gg_tile tile, int comm_programs, gg_group group, int *dev_status,
+                         gg_ag_path path, gg::GatherArgs *out_args, int *vec_bytes, bool *launch)
+{
+    *launch = false;
+    int gi = -1;
+    gg_status st = check_group(heap, group, rank, &gi);
+    if (st != GG_OK)
+        return st;
+    const int es = elem_size(dtype);
+    if (es == 0)
+        return fail(GG_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (path != GG_AG_AUTO && path != GG_AG_BULK && path != GG_AG_VECTOR)
+        return fail(GG_ERR_INVALID_ARG, "unknown path %d", (int)path);
+    if (M < 0 || N < 0)
+        return fail(GG_ERR_INVALID_ARG, "M and N must be >= 0");
+    if (ld_in < N || ld_out < N)
+        return fail(GG_ERR_INVALID_ARG, "ld_in (%lld) and ld_out (%lld) must be >= N (%lld)",
+                    (long long)ld_in, (long long)ld_out, (long long)N);
+    if (tile.block_m < 1 || tile.block_m > 256 || tile.block_n < 1)
+        return fail(GG_ERR_UNSUPPORTED,
+                    "tile %dx%d: block_m must be in [1, 256] and block_n >= 1 (tiles are never "
+                    "remapped)",
+                    tile.block_m, tile.block_n);
+    if ((int64_t)tile.block_m * tile.block_n * es > 32768)
+        return fail(GG_ERR_UNSUPPORTED,
+                    "tile %dx%d of %d-byte elements exceeds 32768 bytes (tiles are never remapped)",
+                    tile.block_m, tile.block_n, es);
+    if (comm_programs < 1 || comm_programs > 65535)
+        return fail(GG_ERR_INVALID_ARG, "comm_programs %d outside [1, 65535]", comm_programs);
+    if (!output || (!input && M > 0 && N > 0))
+        return fail(GG_ERR_INVALID_ARG, "input and output must be non-NULL");
+    if (M == 0 || N == 0)
+        return ok();
+
+    const int W = group.world_size;
+    int64_t rows_out, out_ext, in_ext, tmp;
+    if (!checked_mul(W, M, &rows_out) || !checked_mul(rows_out - 1, ld_out, &tmp) ||
+        !checked_mul(tmp + N, es, &out_ext) || !checked_mul(M - 1, ld_in, &tmp) ||
+        !checked_mul(tmp + N, es, &in_ext))
+        return fail(GG_ERR_INVALID_ARG, "sizes overflow");
+    int64_t out_off;
+    st = symmetric_offset(heap, output, out_ext, "output", &out_off);
+    if (st != GG_OK)
+        return st;
+
+    gg::GatherArgs a{};
+    a.bases = heap->dev_table;
+    a.W = W;
+    a.rank_start = group.rank_start;
+    a.rank_stride = group.rank_stride;
+    uint64_t in_align;
+    if (rank == -1) {
+        int64_t in_off;
+        st = symmetric_offset(heap, input, in_ext, "input", &in_off);
+        if (st != GG_OK)
+            return st;
+        if (overlap(in_off, in_off + in_ext, out_off, out_off + out_ext))
+            return fail(GG_ERR_INVALID_ARG, "input and output overlap inside the partition");
+        a.n_src = W;
+        a.src_first = 0;
+        a.in_abs = nullptr;
+        a.in_off = in_off;
+        in_align = (uint64_t)in_off;
+    } else {
+        const uint64_t i0 = reinterpret_cast<uint64_t>(input);
+        for (int q = 0; q < W; ++q) {
+            const uint64_t o0 = heap->host_bases[group.rank_start + q * group.rank_stride] + out_off;
+            if (overlap(i0, i0 + in_ext, o0, o0 + out_ext))
+                return fail(GG_ERR_INVALID_ARG, "input overlaps the output of member %d", q);
+        }
+        a.n_src = 1;
+        a.src_first = gi;
+        a.in_abs = static_cast<const uint8_t *>(input);
+        a.in_off = 0;
+        in_align = i0;
+    }
+    a.out_off = out_off;
+    a.ld_in_b = ld_in * es;
+    a.ld_out_b = ld_out * es;
+    a.M = M;
+    a.row_b = N * es;
+    a.bm = tile.block_m;
+    a.bn_b = (int64_t)tile.block_n * es;
+    a.tiles_n = ceil_div(N, tile.block_n);
+    a.tiles_per_src = ceil_div(M, tile.block_m) * a.tiles_n;
+    a.total_items = a.tiles_per_src * a.n_src;
+    a.status = dev_status;
+    a.wait_limit_ns = g_wait_limit_ns.load();
+
+    // widest power-of-two granule dividing every address, pitch and length
+    uint64_t g = in_align | (uint64_t)out_off | (uint64_t)a.ld_in_b | (uint64_t)a.ld_out_b |
+                 (uint64_t)a.bn_b | (uint64_t)a.row_b | 16u;
+    const int granule = (int)(g & (~g + 1));  // lowest set bit, <= 16
+    const bool bulk_ok = granule == 16;
+    if (path == GG_AG_BULK && !bulk_ok)
+        return fail(GG_ERR_ALIGNMENT,
+                    "bulk path needs 16-byte aligned input, output, pitches, block_n and N "
+                    "(in bytes)");
+    *vec_bytes = (path == GG_AG_BULK || (path == GG_AG_AUTO && bulk_ok)) ? 0 : granule;
+    *out_args = a;
+    *launch = true;
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+gg_status gg_all_gather_path(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
+                             void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
+                             gg_tile tile, int comm_programs, gg_group group, int *dev_status,
+                             gg_stream_t stream, gg_ag_path path)
+{
+    gg::GatherArgs a;
+    int vec = 0;
+    bool launch = false;
+    gg_status st = prepare_gather(heap, rank, input, ld_in, output, ld_out, M, N, dtype, tile,
+                                  comm_programs, group, dev_status, path, &a, &vec, &launch);
+    if (st != GG_OK || !launch)
+        return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = vec == 0 ? gg::launch_gather_bulk(a, comm_programs, s)
+                             : gg::launch_gather_vec(a, comm_programs, vec, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launching the all-gather");
+    return ok();
+}
+
+gg_status gg_all_gather_check(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
+                              void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
+                              gg_tile tile, int comm_programs, gg_group group, gg_ag_path path,
+                              gg_ag_path *chosen)
+{
+    gg::GatherArgs a;
+    int vec = 0;
+    bool launch = false;
+    gg_status st = prepare_gather(heap, rank, input, ld_in, output, ld_out, M, N, dtype, tile,
+                                  comm_programs, group, nullptr, path, &a, &vec, &launch);
+    if (chosen)
+        *chosen = !launch ? GG_AG_AUTO : (vec == 0 ? GG_AG_BULK : GG_AG_VECTOR);
+    return st;
+}
+
+gg_status gg_all_gather(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
+                        void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
+                        gg_tile tile, int comm_programs, gg_group group, int *dev_status,
+                        gg_stream_t stream)
+{
+    return gg_all_gather_path(heap, rank, input, ld_in, output, ld_out, M, N, dtype, tile,
+                              comm_programs, group, dev_status, stream, GG_AG_AUTO);
+}
+
+}  // extern "C"
+
+namespace {
+
+gg_status prepare_fused(const gg_heap *heap, int rank, const void *A, int64_t lda, const void *B,
+                        int64_t ldb, void *output, int64_t ld_out, int64_t M, int64_t N,
+                        int64_t K, gg_dtype dtype, gg_tile tile, int comm_programs,
+                        gg_group group, int *dev_status, gg::FusedArgs *out_args, bool *launch)
+{
+    *launch = false;
+    int gi = -1;
+    gg_status st = check_group(heap, group, rank, &gi);
+    if (st != GG_OK)
+        return st;
+    if (dtype != GG_F16 && dtype != GG_BF16)
+        return fail(GG_ERR_UNSUPPORTED, "matmul_all_gather takes GG_F16 or GG_BF16");
+    if (tile.block_m != GG_FUSED_BLOCK_M || tile.block_n != GG_FUSED_BLOCK_N)
+        return fail(GG_ERR_UNSUPPORTED,
+                    "fused tile %dx%d is not supported; this build runs %dx%d (tiles are never "
+                    "remapped)",
+                    tile.block_m, tile.block_n, GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N);
+    if (M < 0 || N < 0 || K < 0)
+        return fail(GG_ERR_INVALID_ARG, "M, N and K must be >= 0");
+    if (lda < K || ldb < N || ld_out < N)
+        return fail(GG_ERR_INVALID_ARG, "lda >= K, ldb >= N and ld_out >= N are required");
+    if (comm_programs < 1 || comm_programs > 65535)
+        return fail(GG_ERR_INVALID_ARG, "comm_programs %d outside [1, 65535]", comm_programs);
+    if (!output || ((!A || !B) && M > 0 && N > 0 && K > 0))
+        return fail(GG_ERR_INVALID_ARG, "A, B and output must be non-NULL");
+    if (M == 0 || N == 0 || K == 0)
+        return ok();
+    const uint64_t ua = reinterpret_cast<uint64_t>(A), ub = reinterpret_cast<uint64_t>(B),
+                   uo = reinterpret_cast<uint64_t>(output);
+    if ((ua | ub | uo) % 16 != 0 || lda % 8 || ldb % 8 || ld_out % 8 || N % 8)
+        return fail(GG_ERR_ALIGNMENT,
+                    "A, B and output must be 16-byte aligned; lda, ldb, ld_out and N multiples "
+                    "of 8");
+    if (K > (int64_t)1 << 31 || M > (int64_t)1 << 31 || N > (int64_t)1 << 31)
+        return fail(GG_ERR_UNSUPPORTED, "M, N and K must be below 2^31");
+    const int W = group.world_size;
+    const int64_t out_ext = ((W * M - 1) * ld_out + N) * 2;
+    const int64_t a_ext = ((M - 1) * lda + K) * 2;
+    int64_t out_off;
+    st = symmetric_offset(heap, output, out_ext, "output", &out_off);
+    if (st != GG_OK)
+        return st;
+
+    gg::FusedArgs f{};
+    f.bases = heap->dev_table;
+    f.W = W;
+    f.rank_start = group.rank_start;
+    f.rank_stride = group.rank_stride;
+    f.b = B;
+    f.lda = lda;
+    f.ldb = ldb;
+    f.out_off = out_off;
+    f.ld_out = ld_out;
+    f.M = M;
+    f.N = N;
+    f.K = K;
+    f.is_bf16 = dtype == GG_BF16;
+    f.heap_base = heap->base;
+    f.part_bytes = heap->part;
+    f.num_heaps = heap->H;
+    f.status = dev_status;
+    f.wait_limit_ns = g_wait_limit_ns.load();
+    const uint64_t b_ext = (uint64_t)(((K - 1) * ldb + N) * 2);
+    if (rank == -1) {
+        int64_t a_off;
+        st = symmetric_offset(heap, A, a_ext, "A", &a_off);
+        if (st != GG_OK)
+            return st;
+        if (overlap(a_off, a_off + a_ext, out_off, out_off + out_ext))
+            return fail(GG_ERR_INVALID_ARG, "A and the output overlap inside the partition");
+        f.n_src = W;
+        f.src_first = 0;
+        f.a_abs = nullptr;
+        f.a_off = a_off;
+    } else {
+        for (int q = 0; q < W; ++q) {
+            const uint64_t o0 = heap->host_bases[group.rank_start + q * group.rank_stride] + out_off;
+            if (overlap(ua, ua + a_ext, o0, o0 + out_ext))
+                return fail(GG_ERR_INVALID_ARG, "A overlaps the output of member %d", q);
+        }
+        f.n_src = 1;
+        f.src_first = gi;
+        f.a_abs = A;
+        f.a_off = 0;
+    }
+    for (int q = 0; q < W; ++q) {
+        const uint64_t o0 = heap->host_bases[group.rank_start + q * group.rank_stride] + out_off;
+        if (overlap(ub, ub + b_ext, o0, o0 + out_ext))
+            return fail(GG_ERR_INVALID_ARG, "B overlaps the output of member %d", q);
+    }
+    *out_args = f;
+    *launch = true;
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+gg_status gg_matmul_all_gather(const gg_heap *heap, int rank, const void *A, int64_t lda,
+                               const void *B, int64_t ldb, void *output, int64_t ld_out,
+                               int64_t M, int64_t N, int64_t K, gg_dtype dtype, gg_tile tile,
+                               int comm_programs, gg_group group, int *dev_status,
+                               gg_stream_t stream)
+{
+    gg::FusedArgs f;
+    bool launch = false;
+    gg_status st = prepare_fused(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype, tile,
+                                 comm_programs, group, dev_status, &f, &launch);
+    if (st != GG_OK || !launch)
+        return st;
+    const char *why = nullptr;
+    cudaError_t e = gg::launch_matmul_all_gather(f, comm_programs,
+                                                 reinterpret_cast<cudaStream_t>(stream), &why);
+    if (e != cudaSuccess)
+        return why ? fail(GG_ERR_CUDA, "%s: %s", why, cudaGetErrorName(e))
+                   : cuda_fail(e, "launching matmul_all_gather");
+    return ok();
+}
+
+gg_status gg_matmul_all_gather_check(const gg_heap *heap, int rank, const void *A, int64_t lda,
+                                     const void *B, int64_t ldb, void *output, int64_t ld_out,
+                                     int64_t M, int64_t N, int64_t K, gg_dtype dtype,
+                                     gg_tile tile, int comm_programs, gg_group group)
+{
+    gg::FusedArgs f;
+    bool launch = false;
+    return prepare_fused(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype, tile,
+                         comm_programs, group, nullptr, &f, &launch);
+}
+
+gg_status gg_set_wait_limit_ns(uint64_t ns)
+{
+    g_wait_limit_ns.store(ns == 0 ? kDefaultWaitNs : ns);
+    return ok();
+}
+
+uint64_t gg_get_wait_limit_ns(void) { return g_wait_limit_ns.load(); }
+
+const char *gg_last_error(void) { return g_last_error.c_str(); }
+
+const char *gg_status_string(gg_status s)
+{
+    switch (s) {
+    case GG_OK: return "GG_OK";
+    case GG_ERR_INVALID_ARG: return "GG_ERR_INVALID_ARG";
+    case GG_ERR_ALIGNMENT: return "GG_ERR_ALIGNMENT";
+    case GG_ERR_NOT_IN_HEAP: return "GG_ERR_NOT_IN_HEAP";
+    case GG_ERR_UNSUPPORTED: return "GG_ERR_UNSUPPORTED";
+    case GG_ERR_CUDA: return "GG_ERR_CUDA";
+    case GG_ERR_TIMEOUT: return "GG_ERR_TIMEOUT";
+    }
+    return "GG_UNKNOWN";
+}
+
+int gg_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,62 @@
+// Declarations shared by the library's translation units (host side).
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace gg {
+
+constexpr int kMaxWorld = 64;
+constexpr int kStatusTimeout = -6;  // GG_ERR_TIMEOUT
+
+// One launch of the tiled all-gather.  A "source" is a group member whose
+// M x N block is gathered; a launch covers n_src consecutive group indices
+// starting at src_first.  Work item t (0 <= t < n_src * tiles_per_src) is
+// tile (t mod tiles_per_src) of source src_first + t / tiles_per_src.
+struct GatherArgs {
+    const uint64_t *bases;  // device heap-bases table, one entry per heap
+    int W, rank_start, rank_stride;
+    int n_src, src_first;
+    const uint8_t *in_abs;  // non-null: the one source's block (any device memory)
+    int64_t in_off;         // else: source block at this offset in the member's partition
+    int64_t out_off;        // gathered output at this offset in every member's partition
+    int64_t ld_in_b, ld_out_b;  // row pitches in bytes
+    int64_t M;                  // rows per block
+    int64_t row_b;              // bytes per row (N * element size)
+    int bm;                     // tile rows
+    int64_t bn_b;               // tile row bytes (block_n * element size)
+    int64_t tiles_n, tiles_per_src, total_items;
+    int *status;
+    uint64_t wait_limit_ns;
+};
+
+// Bulk path: 16-byte aligned addresses, pitches, bn_b and row_b.
+cudaError_t launch_gather_bulk(const GatherArgs &a, int programs, cudaStream_t s);
+// Vector path: vec_bytes in {16, 8, 4, 2} divides every address, pitch and row length.
+cudaError_t launch_gather_vec(const GatherArgs &a, int programs, int vec_bytes, cudaStream_t s);
+
+// One launch of the fused matmul + all-gather (see mag_kernel.cu).
+struct FusedArgs {
+    const uint64_t *bases;
+    int W, rank_start, rank_stride;
+    int n_src, src_first;
+    const void *a_abs;     // non-null: the one source's A (any device memory)
+    int64_t a_off;         // else: A at this offset in each member's partition
+    const void *b;         // K x N, shared
+    int64_t lda, ldb;      // elements
+    int64_t out_off;       // gathered output offset in every member's partition
+    int64_t ld_out;        // elements
+    int64_t M, N, K;
+    int is_bf16;
+    // for the A tensor map over all partitions (group launches)
+    uint64_t heap_base;    // device address of partition 0
+    uint64_t part_bytes;
+    int num_heaps;
+    int *status;
+    uint64_t wait_limit_ns;
+};
+
+cudaError_t launch_matmul_all_gather(const FusedArgs &a, int programs, cudaStream_t s,
+                                     const char **why);
+
+}  // namespace gg

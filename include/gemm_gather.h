@@ -1,0 +1,219 @@
+/*
+ * gemm_gather — tiled all-gather over a symmetric heap, alone and fused into
+ * the epilogue of a matmul, for one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Plain pointers and sizes only.  All device memory is owned by the
+ * caller; the library never allocates device memory and keeps no state on
+ * the device.  Every call that launches work is asynchronous on the caller's
+ * stream.  Errors found on the host are returned before anything is
+ * launched; gg_last_error() then describes them.  No call aborts the process.
+ *
+ * Logical ranks.  On one GPU the W ranks of a group are logical: H equal
+ * partitions ("heaps") of one device allocation, reached through a table of
+ * heap base addresses, the way the ROCm/iris pages validate their kernels on
+ * a single GPU (iris #594, "Local validation": independent allocations stand
+ * for ranks).  A symmetric buffer sits at the same byte offset in every
+ * partition (iris PR #626, "Summary": peer address = local address +
+ * (peer base - local base)).
+ *
+ * Group (iris #591 "Gluon all-gather reloads peer heap bases inside the tile
+ * loop", Description §1): member i of a group is heap
+ * rank_start + i * rank_stride, for i in [0, world_size).  Heaps outside the
+ * group are never touched.
+ *
+ * Gather (iris #594, "Multi-GPU CI": same result as
+ * torch.distributed.all_gather_into_tensor): the gathered output of every
+ * member d is world_size*M x N; row block i (rows i*M .. i*M+M-1) is member
+ * i's M x N input.  Elements are copied bit for bit.  Columns N..ld_out-1 of
+ * the output (padding) are never written.
+ */
+#ifndef GEMM_GATHER_H
+#define GEMM_GATHER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st *gg_stream_t;
+
+typedef enum {
+    GG_OK = 0,
+    GG_ERR_INVALID_ARG = -1,  /* bad size, rank, group, pitch or overlap     */
+    GG_ERR_ALIGNMENT = -2,    /* pointer/pitch alignment a path requires     */
+    GG_ERR_NOT_IN_HEAP = -3,  /* a symmetric buffer does not fit a partition */
+    GG_ERR_UNSUPPORTED = -4,  /* valid request this build does not implement */
+    GG_ERR_CUDA = -5,         /* a CUDA runtime call failed                  */
+    GG_ERR_TIMEOUT = -6       /* device: a bounded wait gave up (status word)*/
+} gg_status;
+
+typedef enum { GG_F16 = 0, GG_BF16 = 1, GG_F32 = 2 } gg_dtype;
+
+/* Tile shape.  Always explicit: the library has no default tile and never
+ * replaces the one it is given (iris #594, "Reviewer performance evaluation":
+ * a launcher that remapped an explicit 32x64 tile to 8x256 made 32x64
+ * impossible to run).  A shape a kernel cannot run returns
+ * GG_ERR_UNSUPPORTED. */
+typedef struct { int block_m, block_n; } gg_tile;
+
+/* Process group over heap indices (see above). */
+typedef struct { int rank_start, rank_stride, world_size; } gg_group;
+
+typedef struct gg_heap gg_heap; /* opaque host handle */
+
+/* Largest world_size a call accepts, and largest number of heaps. */
+#define GG_MAX_WORLD 64
+#define GG_MAX_HEAPS 1024
+
+/* Supported fused (matmul_all_gather) tile: the tcgen05 tile of one CTA. */
+#define GG_FUSED_BLOCK_M 128
+#define GG_FUSED_BLOCK_N 256
+
+/* ---------------------------------------------------------------------------
+ * gg_heap_create — describe a symmetric heap of `num_heaps` partitions of
+ * `bytes_per_rank` bytes each, laid out back to back from `dev_base`
+ * (device memory, caller-owned, at least num_heaps*bytes_per_rank bytes), and
+ * write the heap-bases table: entry h = dev_base + h*bytes_per_rank, as
+ * uint64, into `dev_bases_table` (device memory, caller-owned, num_heaps
+ * entries).  The table write is a copy enqueued on `stream`; it is ordered
+ * before any later gather or fused call on that stream.  (iris PR #626
+ * "Summary" and iris #591 Description §1: heap_bases.)
+ * Requirements: dev_base 256-byte aligned; bytes_per_rank a positive multiple
+ * of 256; 1 <= num_heaps <= GG_MAX_HEAPS.  On success *out is a new handle
+ * (host memory only), released by gg_heap_destroy.
+ * ------------------------------------------------------------------------- */
+gg_status gg_heap_create(void *dev_base, size_t bytes_per_rank, int num_heaps,
+                         uint64_t *dev_bases_table, gg_stream_t stream, gg_heap **out);
+
+/* gg_heap_wrap — the same handle as gg_heap_create, without writing the
+ * device table: for callers that write or share the table themselves (its
+ * contents must then equal gg_heap_bases before the first launch).  Touches
+ * no device state, so it also serves host-only validation with the
+ * *_check entry points below. */
+gg_status gg_heap_wrap(void *dev_base, size_t bytes_per_rank, int num_heaps,
+                       uint64_t *dev_bases_table, gg_heap **out);
+
+/* Copy the heap-bases table (host copy kept by the handle) into host_out[0..n). */
+gg_status gg_heap_bases(const gg_heap *heap, uint64_t *host_out, int n);
+
+/* Number of partitions and partition size of a heap. */
+gg_status gg_heap_info(const gg_heap *heap, int *num_heaps, size_t *bytes_per_rank);
+
+/* Release the host handle (device memory stays the caller's). NULL is a no-op. */
+gg_status gg_heap_destroy(gg_heap *heap);
+
+/* ---------------------------------------------------------------------------
+ * gg_all_gather — the persistent tiled all-gather (iris PR #626, "Triton CCL
+ * all-gather"; iris #594, "PR description"; iris #591, Description §1).
+ *
+ * rank >= 0: heap `rank` (a member of `group`, group index i) contributes:
+ *   `input` (any device pointer, M x N, row pitch ld_in elements) is written
+ *   into row block i of the output of every member, itself first.
+ * rank == -1: every member contributes in one launch; `input` must then be a
+ *   symmetric heap buffer (the byte offset of `input` within its partition is
+ *   used in every member's partition).
+ * `output` is a symmetric heap buffer: a pointer into any partition; its byte
+ *   offset within that partition locates the world_size*M x N output (row
+ *   pitch ld_out elements) in every member's partition.  The whole output
+ *   must fit inside a partition (else GG_ERR_NOT_IN_HEAP) and must not
+ *   overlap the input (else GG_ERR_INVALID_ARG).
+ * tile: block_m rows x block_n columns of one work item; each work item is
+ *   read once and stored to every member, the local copy first and the peers
+ *   in rotated order (i+1, i+2, ... mod world_size; iris PR #626, "Summary").
+ *   block_m in [1, 256], block_n >= 1, block_m*block_n*elem_size <= 32768.
+ * comm_programs: number of persistent programs (CTAs) of the launch, 1..65535;
+ *   for rank == -1 they share all world_size x tiles work items.
+ * dev_status: nullable device int; if a bounded wait inside the kernel gives
+ *   up, GG_ERR_TIMEOUT is stored there (first error wins; the caller zeroes
+ *   it).  M == 0 or N == 0 launches nothing and returns GG_OK.
+ * Any alignment is accepted: 16-byte aligned pointers and pitches take the
+ *   bulk-copy path, others a narrower vector path.  Results are identical.
+ * ------------------------------------------------------------------------- */
+gg_status gg_all_gather(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
+                        void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
+                        gg_tile tile, int comm_programs, gg_group group, int *dev_status,
+                        gg_stream_t stream);
+
+/* Data-path variants of gg_all_gather (same arguments and result):
+ *   GG_AG_AUTO      bulk path when aligned, else vector path (gg_all_gather)
+ *   GG_AG_BULK      tiles staged in shared memory by bulk copies (TMA engine),
+ *                   stored to each destination by bulk copies; needs 16-byte
+ *                   aligned pointers, pitches, block_n*elem_size and
+ *                   N*elem_size (else GG_ERR_ALIGNMENT)
+ *   GG_AG_VECTOR    16/8/4/2-byte vector loads into registers, then one vector
+ *                   store per destination (widest width the alignment allows)
+ */
+typedef enum { GG_AG_AUTO = 0, GG_AG_BULK = 1, GG_AG_VECTOR = 2 } gg_ag_path;
+
+gg_status gg_all_gather_path(const gg_heap *heap, int rank, const void *input,
+                             int64_t ld_in, void *output, int64_t ld_out, int64_t M,
+                             int64_t N, gg_dtype dtype, gg_tile tile, int comm_programs,
+                             gg_group group, int *dev_status, gg_stream_t stream,
+                             gg_ag_path path);
+
+/* Validate a gg_all_gather_path call exactly as the launching call does and
+ * launch nothing.  *chosen (nullable) receives the path a launch would take
+ * (GG_AG_BULK or GG_AG_VECTOR; GG_AG_AUTO when there is nothing to launch). */
+gg_status gg_all_gather_check(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
+                              void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
+                              gg_tile tile, int comm_programs, gg_group group, gg_ag_path path,
+                              gg_ag_path *chosen);
+
+/* ---------------------------------------------------------------------------
+ * gg_matmul_all_gather — the fused form (iris PR #626, "Summary" and
+ * "Benchmark": the matmul's epilogue all-gathers each output tile).
+ * Member r computes C_r = A_r @ B (A_r: M x K row-major, row pitch lda;
+ * B: K x N row-major, row pitch ldb, one buffer shared by all members),
+ * accumulating in float32 on the tensor cores, rounds C_r to `dtype`
+ * (round to nearest even) and writes it into row block i (its group index)
+ * of the world_size*M x N output of every member, local copy first.
+ * dtype: GG_F16 or GG_BF16 (A, B and the output share it).
+ * rank >= 0: only that member computes and gathers its block; `A` is any
+ *   device pointer.  rank == -1: every member, in one launch; `A` is then a
+ *   symmetric heap buffer.
+ * tile: must be {GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N}; anything else returns
+ *   GG_ERR_UNSUPPORTED (never remapped).
+ * Alignment (GG_ERR_ALIGNMENT otherwise): A, B, output 16-byte aligned;
+ *   lda, ldb, ld_out multiples of 8; N a multiple of 8.
+ * comm_programs: number of persistent CTAs (one per SM at most is useful).
+ * M, N or K == 0: nothing is launched, GG_OK (with K == 0 nothing is
+ *   written either).
+ * ------------------------------------------------------------------------- */
+gg_status gg_matmul_all_gather(const gg_heap *heap, int rank, const void *A, int64_t lda,
+                               const void *B, int64_t ldb, void *output, int64_t ld_out,
+                               int64_t M, int64_t N, int64_t K, gg_dtype dtype,
+                               gg_tile tile, int comm_programs, gg_group group,
+                               int *dev_status, gg_stream_t stream);
+
+/* Validate a gg_matmul_all_gather call exactly as the launching call does
+ * and launch nothing. */
+gg_status gg_matmul_all_gather_check(const gg_heap *heap, int rank, const void *A, int64_t lda,
+                                     const void *B, int64_t ldb, void *output, int64_t ld_out,
+                                     int64_t M, int64_t N, int64_t K, gg_dtype dtype,
+                                     gg_tile tile, int comm_programs, gg_group group);
+
+/* ---------------------------------------------------------------------------
+ * Bounded waits.  Every wait of a kernel on an mbarrier gives up after this
+ * many nanoseconds of wall time (default 2e9), stores GG_ERR_TIMEOUT in the
+ * call's dev_status, drains the copies it has in flight and returns.  Applies
+ * to launches made after the call, from any thread.  0 restores the default.
+ * ------------------------------------------------------------------------- */
+gg_status gg_set_wait_limit_ns(uint64_t ns);
+uint64_t gg_get_wait_limit_ns(void);
+
+/* Message describing the last error returned on this thread ("" if none). */
+const char *gg_last_error(void);
+
+/* Short name of a status code. */
+const char *gg_status_string(gg_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int gg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GEMM_GATHER_H */

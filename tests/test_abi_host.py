@@ -1,0 +1,183 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads, exports
+every entry point the header declares, and validates arguments exactly as
+documented, without launching anything (gg_heap_wrap + the *_check entry
+points touch no device state)."""
+import ctypes
+import json
+import os
+import re
+
+import pytest
+import torch
+
+import gemm_gather_gb300 as gg
+from gemm_gather_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gemm_gather.h")
+BASE = 1 << 36          # fake device addresses: nothing is dereferenced
+TABLE = 1 << 40
+PART = 1 << 24
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:gg_status|const char \*|uint64_t|int)\s*\*?\s*(gg_\w+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 14
+    lib = ctypes.CDLL(_lib.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(_lib.EXPORTS) == names
+
+
+@pytest.fixture
+def heap():
+    return gg.heap_wrap(BASE, PART, 8, TABLE)
+
+
+def test_heap_wrap_table(heap):
+    assert gg.heap_info(heap) == (8, PART)
+    assert gg.heap_bases(heap) == [BASE + h * PART for h in range(8)]
+
+
+@pytest.mark.parametrize("args,status", [
+    ((BASE + 8, PART, 4, TABLE), _lib.GG_ERR_ALIGNMENT),
+    ((BASE, PART + 8, 4, TABLE), _lib.GG_ERR_INVALID_ARG),
+    ((BASE, 0, 4, TABLE), _lib.GG_ERR_INVALID_ARG),
+    ((BASE, PART, 0, TABLE), _lib.GG_ERR_INVALID_ARG),
+    ((BASE, PART, 2000, TABLE), _lib.GG_ERR_INVALID_ARG),
+    ((0, PART, 4, TABLE), _lib.GG_ERR_INVALID_ARG),
+    ((BASE, PART, 4, TABLE + 4), _lib.GG_ERR_ALIGNMENT),
+])
+def test_heap_wrap_rejects(args, status):
+    with pytest.raises(gg.GGError) as e:
+        gg.heap_wrap(*args)
+    assert e.value.status == status
+
+
+def ag(heap, **kw):
+    a = dict(rank=-1, input=BASE + 4096, ld_in=256, output=BASE + (1 << 20), ld_out=256, M=64,
+             N=256, dtype=torch.float16, tile=(8, 256), comm_programs=4, group=(0, 1, 2),
+             path="auto")
+    a.update(kw)
+    return gg.all_gather_check(heap, a["rank"], a["input"], a["ld_in"], a["output"], a["ld_out"],
+                               a["M"], a["N"], a["dtype"], a["tile"], a["comm_programs"],
+                               a["group"], a["path"])
+
+
+def test_gather_valid_calls(heap):
+    assert ag(heap) == "bulk"
+    assert ag(heap, rank=1) == "bulk"
+    assert ag(heap, M=0) == "none"
+    assert ag(heap, N=0) == "none"
+    assert ag(heap, input=BASE + 4098) == "vector"
+    assert ag(heap, path="vector") == "vector"
+    assert ag(heap, group=(1, 2, 4), rank=5) == "bulk"
+    assert ag(heap, N=255, ld_in=256, ld_out=256) == "vector"
+    # an explicit 32x64 tile is accepted as given (never remapped)
+    assert ag(heap, tile=(32, 64)) == "bulk"
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(group=(0, 1, 9)), _lib.GG_ERR_INVALID_ARG),          # member 8 is not a heap
+    (dict(group=(0, 0, 2)), _lib.GG_ERR_INVALID_ARG),          # stride 0
+    (dict(group=(0, 1, 0)), _lib.GG_ERR_INVALID_ARG),          # empty group
+    (dict(group=(-1, 1, 2)), _lib.GG_ERR_INVALID_ARG),
+    (dict(group=(0, 1, 65)), _lib.GG_ERR_INVALID_ARG),         # above GG_MAX_WORLD
+    (dict(rank=3), _lib.GG_ERR_INVALID_ARG),                   # not a member
+    (dict(rank=-2), _lib.GG_ERR_INVALID_ARG),
+    (dict(group=(1, 2, 3), rank=2), _lib.GG_ERR_INVALID_ARG),  # between strided members
+    (dict(ld_in=100), _lib.GG_ERR_INVALID_ARG),                # pitch below N
+    (dict(ld_out=100), _lib.GG_ERR_INVALID_ARG),
+    (dict(M=-1), _lib.GG_ERR_INVALID_ARG),
+    (dict(tile=(0, 256)), _lib.GG_ERR_UNSUPPORTED),
+    (dict(tile=(257, 8)), _lib.GG_ERR_UNSUPPORTED),
+    (dict(tile=(64, 512)), _lib.GG_ERR_UNSUPPORTED),           # 64 KB tile
+    (dict(comm_programs=0), _lib.GG_ERR_INVALID_ARG),
+    (dict(comm_programs=70000), _lib.GG_ERR_INVALID_ARG),
+    (dict(output=BASE - 256), _lib.GG_ERR_NOT_IN_HEAP),        # below the heap
+    (dict(output=BASE + 8 * PART), _lib.GG_ERR_NOT_IN_HEAP),   # past the end
+    (dict(output=BASE + PART - 1024), _lib.GG_ERR_NOT_IN_HEAP),  # overruns the partition
+    (dict(input=BASE + 8 * PART + (1 << 20)), _lib.GG_ERR_NOT_IN_HEAP),
+    (dict(input=BASE + (1 << 20) + 512), _lib.GG_ERR_INVALID_ARG),  # overlaps the output
+    (dict(rank=0, input=BASE + PART + (1 << 20)), _lib.GG_ERR_INVALID_ARG),  # overlaps member 1
+    (dict(input=BASE + 4098, path="bulk"), _lib.GG_ERR_ALIGNMENT),
+    (dict(dtype=7), _lib.GG_ERR_INVALID_ARG),
+    (dict(output=0), _lib.GG_ERR_INVALID_ARG),
+])
+def test_gather_rejects(heap, kw, status):
+    with pytest.raises(gg.GGError) as e:
+        ag(heap, **kw)
+    assert e.value.status == status, str(e.value)
+    assert gg.lib.gg_last_error().decode()
+
+
+def mag(heap, **kw):
+    a = dict(rank=-1, A=BASE + 4096, lda=1024, B=TABLE + 4096, ldb=512, output=BASE + (4 << 20),
+             ld_out=512, M=256, N=512, K=1024, dtype=torch.float16, tile=gg.FUSED_TILE,
+             comm_programs=148, group=(0, 1, 4))
+    a.update(kw)
+    gg.matmul_all_gather_check(heap, a["rank"], a["A"], a["lda"], a["B"], a["ldb"], a["output"],
+                               a["ld_out"], a["M"], a["N"], a["K"], a["dtype"], a["tile"],
+                               a["comm_programs"], a["group"])
+
+
+def test_fused_valid_calls(heap):
+    mag(heap)
+    mag(heap, rank=2, A=TABLE + (1 << 20))
+    mag(heap, dtype=torch.bfloat16)
+    mag(heap, K=0)
+    mag(heap, M=0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(tile=(256, 128)), _lib.GG_ERR_UNSUPPORTED),
+    (dict(tile=(32, 64)), _lib.GG_ERR_UNSUPPORTED),    # never remapped to the supported tile
+    (dict(tile=(8, 256)), _lib.GG_ERR_UNSUPPORTED),
+    (dict(dtype=torch.float32), _lib.GG_ERR_UNSUPPORTED),
+    (dict(N=500, ldb=512, ld_out=512), _lib.GG_ERR_ALIGNMENT),
+    (dict(lda=1028), _lib.GG_ERR_ALIGNMENT),
+    (dict(A=BASE + 4100), _lib.GG_ERR_ALIGNMENT),
+    (dict(lda=1000), _lib.GG_ERR_INVALID_ARG),          # below K
+    (dict(group=(0, 1, 9)), _lib.GG_ERR_INVALID_ARG),
+    (dict(rank=5), _lib.GG_ERR_INVALID_ARG),
+    (dict(output=BASE + PART - 4096), _lib.GG_ERR_NOT_IN_HEAP),
+    (dict(A=TABLE), _lib.GG_ERR_NOT_IN_HEAP),           # group launch: A must be symmetric
+    (dict(A=BASE + (4 << 20) + 4096), _lib.GG_ERR_INVALID_ARG),  # A overlaps the output
+    (dict(B=BASE + (4 << 20)), _lib.GG_ERR_INVALID_ARG),         # B overlaps member 0's output
+])
+def test_fused_rejects(heap, kw, status):
+    with pytest.raises(gg.GGError) as e:
+        mag(heap, **kw)
+    assert e.value.status == status, str(e.value)
+
+
+def test_wait_limit_roundtrip():
+    gg.set_wait_limit_ns(12345)
+    assert gg.get_wait_limit_ns() == 12345
+    gg.set_wait_limit_ns(0)
+    assert gg.get_wait_limit_ns() == 2_000_000_000
+
+
+def test_page_facts_tile_geometry():
+    """The tile geometry the pages print (tests/golden/page_facts.json)."""
+    facts = json.load(open(os.path.join(ROOT, "tests", "golden", "page_facts.json")))
+    for t in facts["tiles"]:
+        es = {"f16": 2}[t["dtype"]]
+        assert t["block_m"] * t["block_n"] == t["elements"]
+        assert t["block_n"] * es == t["row_bytes"]
+    heap = gg.heap_wrap(BASE, PART, 8, TABLE)
+    t = facts["explicit_tile_not_remapped"]
+    # accepted as the 32x64 tile it is: the bulk path needs block_n*2 % 16 == 0 (128 B rows)
+    assert ag(heap, tile=(t["block_m"], t["block_n"])) == "bulk"
+    s = facts["sweep"]
+    assert len(s["M"]) * len(s["N"]) * len(s["dtypes"]) * len(s["comm_sms"]) == s["configurations"]
+    p = facts["peers_per_tile"]
+    assert p["world_size"] - 1 == p["peer_destinations"]
+    r = facts["rotated_order"]
+    assert [(r["rank"] + j) % r["world_size"] for j in range(r["world_size"])] == r["order"]

@@ -1,0 +1,85 @@
+"""Bounded waits on the GPU: with the wait limit forced down to 1 ns, a wait
+inside each kernel gives up, the kernel stores GG_ERR_TIMEOUT in the status
+word, drains its copies in flight and returns; the context stays usable and a
+normal launch right after gives the oracle's result.  Nothing here faults,
+traps or hangs the GPU: the waits end on their own limit."""
+import numpy as np
+import pytest
+import torch
+
+import gg_inputs
+from tests import heap_image as hi
+from tests.gpu_util import device_heap, download, first_diff
+
+pytestmark = pytest.mark.gpu
+
+TIMEOUT = -6
+
+
+@pytest.fixture
+def short_waits():
+    import gemm_gather_gb300 as gg
+    gg.set_wait_limit_ns(1)
+    yield
+    gg.set_wait_limit_ns(0)  # back to the default
+
+
+def _gather_heap():
+    lay = hi.make_layout(4, 4, 512, 4096, 2)
+    host = hi.sentinel_heap(lay)
+    for h in range(4):
+        hi.put_block(host, lay, h, gg_inputs.index_coded(h, 512, 4096, 2).numpy(), lay.in_off,
+                     lay.ld_in)
+    return lay, host
+
+
+def test_gather_wait_limit_reports_timeout(oracle, short_waits):
+    import gemm_gather_gb300 as gg
+    lay, host = _gather_heap()
+    sh = device_heap(lay, host)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gg.all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), lay.ld_in, sh.ptr(0, lay.out_off),
+                  lay.ld_out, lay.M, lay.N, torch.float16, (8, 256), 4, (0, 1, 4),
+                  status=status, path="bulk")
+    torch.cuda.synchronize()
+    assert int(status.item()) == TIMEOUT
+    # the context is intact: a normal launch gives the oracle's heap
+    gg.set_wait_limit_ns(0)
+    status.zero_()
+    gg.all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), lay.ld_in, sh.ptr(0, lay.out_off),
+                  lay.ld_out, lay.M, lay.N, torch.float16, (8, 256), 4, (0, 1, 4),
+                  status=status, path="bulk")
+    got = download(sh)
+    assert int(status.item()) == 0
+    oracle.all_gather(host, lay.part_bytes, lay.in_off, lay.ld_in, lay.out_off, lay.ld_out,
+                      lay.M, lay.N, 2, (0, 1, 4))
+    assert np.array_equal(got, host), first_diff(got, host, lay)
+
+
+def test_fused_wait_limit_reports_timeout(oracle, short_waits):
+    import gemm_gather_gb300 as gg
+    W, M, N, K = 2, 512, 1024, 2048
+    lay = hi.make_layout(W, W, M, N, 2, ld_in=K)
+    host = hi.sentinel_heap(lay)
+    gen = gg_inputs.generator(1)
+    for h in range(W):
+        a = gg_inputs.integers((M, K), -2, 2, torch.float16, gen)
+        hi.put_block(host, lay, h, a.view(torch.int16).numpy(), lay.in_off, K)
+    B = gg_inputs.integers((K, N), -2, 2, torch.float16, gen)
+    sh = device_heap(lay, host)
+    Bd = B.to("cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gg.matmul_all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), K, Bd, N, sh.ptr(0, lay.out_off), N,
+                         M, N, K, torch.float16, gg.FUSED_TILE, 8, (0, 1, W), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == TIMEOUT
+    gg.set_wait_limit_ns(0)
+    status.zero_()
+    gg.matmul_all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), K, Bd, N, sh.ptr(0, lay.out_off), N,
+                         M, N, K, torch.float16, gg.FUSED_TILE, 8, (0, 1, W), status=status)
+    got = download(sh)
+    assert int(status.item()) == 0
+    oracle.matmul_all_gather(host, lay.part_bytes, lay.in_off, K,
+                             B.view(torch.int16).numpy().view(np.uint16), lay.out_off, N, M, N, K,
+                             0, (0, 1, W))
+    assert np.array_equal(got, host), first_diff(got, host, lay)

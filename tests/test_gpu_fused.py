@@ -1,0 +1,142 @@
+"""Parity of the fused tcgen05 matmul + all-gather with the oracle, through
+the C ABI.
+
+* Integer-valued operands: every product and partial sum is an exact integer
+  in float32, so the device result must equal the oracle's bit for bit, over
+  the WHOLE heap (outputs, padding, guards, inputs, inactive heaps).
+* Random operands (normal / sqrt(K)): every value within
+  5e-3 * RMS(reference row) of the float64 reference, plus half an ulp of the
+  output type for the final rounding; every byte outside the outputs
+  untouched; the W copies of each block bit-identical.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gg_inputs
+from tests import heap_image as hi
+from tests.gpu_util import device_heap, download, first_diff
+
+pytestmark = pytest.mark.gpu
+
+FMT = {torch.float16: 0, torch.bfloat16: 1}
+MANT = {torch.float16: 10, torch.bfloat16: 7}  # stored fraction bits
+REL_TOL = 5e-3
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def half_ulp(x: np.ndarray, dtype) -> np.ndarray:
+    """Half an ulp of the 16-bit type at |x| (normal range)."""
+    ax = np.maximum(np.abs(x), 2.0 ** -14)
+    e = np.floor(np.log2(ax))
+    return np.ldexp(1.0, (e - MANT[dtype] - 1).astype(np.int64))
+
+
+def check_tolerance(gpu_vals: np.ndarray, ref: np.ndarray, dtype) -> None:
+    rms = np.sqrt(np.mean(ref ** 2, axis=1, keepdims=True))
+    bound = REL_TOL * rms + np.maximum(half_ulp(ref, dtype), half_ulp(gpu_vals, dtype))
+    err = np.abs(gpu_vals - ref)
+    bad = err > bound
+    assert not bad.any(), (f"{int(bad.sum())} values outside tolerance; worst "
+                           f"{float((err / bound).max()):.3f} x bound")
+
+
+def run_fused(oracle, H, group, M, N, K, dtype, programs, values="int", lda_pad=0,
+              ld_out_pad=0, mode="group", seed=0):
+    import gemm_gather_gb300 as gg
+    start, stride, W = group
+    members = [start + i * stride for i in range(W)]
+    lda = K + lda_pad
+    lay = hi.make_layout(H, W, M, N, 2, ld_in=lda, ld_out=N + ld_out_pad)
+    host = hi.sentinel_heap(lay)
+    gen = gg_inputs.generator(seed)
+    A = {}
+    for h in range(H):
+        if values == "int":
+            t = gg_inputs.integers((M, K), -2, 2, dtype, gen)
+        else:
+            t = gg_inputs.normal((M, K), dtype, gen, scale=K ** -0.5)
+        if h in members:
+            A[h] = t
+            hi.put_block(host, lay, h, _bits(t), lay.in_off, lda)
+    if values == "int":
+        B = gg_inputs.integers((K, N), -2, 2, dtype, gen)
+    else:
+        B = gg_inputs.normal((K, N), dtype, gen, scale=K ** -0.5)
+    sh = device_heap(lay, host)
+    Bd = B.to("cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    if mode == "group":
+        gg.matmul_all_gather(sh.heap, -1, sh.ptr(members[0], lay.in_off), lda, Bd, N,
+                             sh.ptr(members[0], lay.out_off), lay.ld_out, M, N, K, dtype,
+                             gg.FUSED_TILE, programs, group, status=status)
+    else:
+        for h in members:
+            gg.matmul_all_gather(sh.heap, h, sh.ptr(h, lay.in_off), lda, Bd, N,
+                                 sh.ptr(h, lay.out_off), lay.ld_out, M, N, K, dtype,
+                                 gg.FUSED_TILE, programs, group, status=status)
+    got = download(sh)
+    assert int(status.item()) == 0, int(status.item())
+    prods = oracle.matmul_all_gather(host, lay.part_bytes, lay.in_off, lda, _bits(B),
+                                     lay.out_off, lay.ld_out, M, N, K, FMT[dtype], group)
+    if values == "int":
+        assert np.array_equal(got, host), first_diff(got, host, lay)
+        return
+    mask = hi.output_mask(lay, members)
+    assert np.array_equal(got[~mask], host[~mask]), "bytes outside the outputs changed"
+    outs = [hi.get_block(got, lay, d, lay.out_off, W * M, lay.ld_out, N, np.uint16)
+            for d in members]
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0]), "destination copies differ"
+    vals = torch.from_numpy(outs[0].view(np.int16)).view(dtype).to(torch.float64).numpy()
+    for i in range(W):
+        check_tolerance(vals[i * M:(i + 1) * M], prods[i], dtype)
+
+
+# (H, group, M, N, K, programs, lda_pad, ld_out_pad)
+INT_CASES = [
+    (2, (0, 1, 2), 128, 256, 64, 2, 0, 0),        # one tile, one K block
+    (2, (0, 1, 2), 128, 256, 192, 2, 0, 0),       # ring of 3 stages filled once
+    (2, (0, 1, 2), 128, 256, 640, 1, 0, 0),       # ring wraps; one CTA
+    (2, (0, 1, 2), 128, 256, 100, 2, 0, 0),       # ragged K
+    (2, (0, 1, 2), 200, 264, 72, 4, 8, 16),       # ragged M, N, K; padded pitches
+    (3, (0, 1, 3), 300, 520, 320, 5, 0, 8),       # several tiles per CTA
+    (8, (0, 2, 4), 64, 512, 128, 3, 0, 0),        # strided subgroup, inactive heaps
+    (8, (1, 2, 4), 129, 256, 64, 148, 0, 0),      # subgroup from heap 1, more CTAs than tiles
+    (4, (0, 1, 4), 256, 768, 256, 1, 0, 0),       # one CTA walks 24 tiles (TMEM phases)
+    (1, (0, 1, 1), 8, 8, 16, 1, 0, 0),            # tiny, W = 1
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("case", INT_CASES, ids=lambda c: f"H{c[0]}g{c[1]}_{c[2]}x{c[3]}x{c[4]}p{c[5]}")
+def test_integer_operands_bit_exact(oracle, case, dtype):
+    H, group, M, N, K, programs, lp, op = case
+    run_fused(oracle, H, group, M, N, K, dtype, programs, "int", lp, op)
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("shape", [(256, 512, 1024), (130, 264, 520), (512, 1024, 2048)])
+def test_random_operands_within_tolerance(oracle, shape, dtype):
+    M, N, K = shape
+    run_fused(oracle, 3, (0, 1, 3), M, N, K, dtype, 7, "normal")
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+def test_single_rank_launches(oracle, dtype):
+    run_fused(oracle, 4, (0, 1, 4), 160, 512, 192, dtype, 5, "int", mode="ranks")
+    run_fused(oracle, 6, (1, 2, 3), 96, 256, 320, dtype, 3, "normal", mode="ranks")
+
+
+def test_zero_k_writes_nothing():
+    import gemm_gather_gb300 as gg
+    lay = hi.make_layout(2, 2, 128, 256, 2, ld_in=64)
+    host = hi.sentinel_heap(lay)
+    sh = device_heap(lay, host)
+    B = torch.zeros((1, 256), dtype=torch.float16, device="cuda")
+    gg.matmul_all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), 64, B, 256, sh.ptr(0, lay.out_off),
+                         256, 128, 256, 0, torch.float16, gg.FUSED_TILE, 4, (0, 1, 2))
+    assert np.array_equal(download(sh), host)
