@@ -21,7 +21,7 @@ from ._lib import (GG_AG_AUTO, GG_AG_BULK, GG_AG_VECTOR, GG_BF16, GG_ERR_ALIGNME
 __all__ = [
     "heap_create", "heap_wrap", "heap_bases", "heap_info", "heap_destroy", "all_gather",
     "all_gather_check", "matmul_all_gather", "matmul_all_gather_check", "set_wait_limit_ns",
-    "get_wait_limit_ns", "SymmetricHeap", "Heap", "GGError", "DTYPE_CODES", "PATHS",
+    "get_wait_limit_ns", "debug_inject_stall", "SymmetricHeap", "Heap", "GGError", "DTYPE_CODES", "PATHS",
     "FUSED_TILE",
 ]
 
@@ -145,6 +145,10 @@ def set_wait_limit_ns(ns: int) -> None:
 
 def get_wait_limit_ns() -> int:
     return int(lib.gg_get_wait_limit_ns())
+
+
+def debug_inject_stall(enable: bool) -> None:
+    check(lib.gg_debug_inject_stall(1 if enable else 0))
 
 
 # --------------------------------------------------------------------------- #

@@ -30,7 +30,7 @@ EXPORTS = (
     "gg_heap_create", "gg_heap_wrap", "gg_heap_bases", "gg_heap_info", "gg_heap_destroy",
     "gg_all_gather", "gg_all_gather_path", "gg_all_gather_check",
     "gg_matmul_all_gather", "gg_matmul_all_gather_check",
-    "gg_set_wait_limit_ns", "gg_get_wait_limit_ns",
+    "gg_set_wait_limit_ns", "gg_get_wait_limit_ns", "gg_debug_inject_stall",
     "gg_last_error", "gg_status_string", "gg_version",
 )
 
@@ -66,6 +66,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
                                         Tile, i32, Group], i32),
         "gg_set_wait_limit_ns": ([u64], i32),
         "gg_get_wait_limit_ns": ([], u64),
+        "gg_debug_inject_stall": ([i32], i32),
         "gg_last_error": ([], ctypes.c_char_p),
         "gg_status_string": ([i32], ctypes.c_char_p),
         "gg_version": ([], i32),

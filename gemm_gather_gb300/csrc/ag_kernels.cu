@@ -111,6 +111,8 @@ __global__ void __launch_bounds__(kAgWarps * 32)
         const int st = (int)(k % stages);
         const uint32_t bar = full0 + 8u * st;
         const uint32_t buf = ring + (uint32_t)st * stage_bytes;
+        if (a.inject_stall && k == 0 && blockIdx.x == 0 && warp == 0)
+            return;  // test hook: this stage's barrier phase never completes
         if (lane == 0)
             ptx::mbar_arrive_expect_tx(bar, (uint32_t)it.rows * it.rb);
         __syncwarp();

@@ -24,6 +24,7 @@ namespace {
 
 thread_local std::string g_last_error;
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_inject_stall{0};
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 gg_status fail(gg_status s, const char *fmt, ...)
@@ -293,6 +294,7 @@ gg_status prepare_gather(const gg_heap *heap, int rank, const void *input, int64
     a.total_items = a.tiles_per_src * a.n_src;
     a.status = dev_status;
     a.wait_limit_ns = g_wait_limit_ns.load();
+    a.inject_stall = g_inject_stall.load();
 
     // widest power-of-two granule dividing every address, pitch and length
     uint64_t g = in_align | (uint64_t)out_off | (uint64_t)a.ld_in_b | (uint64_t)a.ld_out_b |
@@ -423,6 +425,7 @@ gg_status prepare_fused(const gg_heap *heap, int rank, const void *A, int64_t ld
     f.num_heaps = heap->H;
     f.status = dev_status;
     f.wait_limit_ns = g_wait_limit_ns.load();
+    f.inject_stall = g_inject_stall.load();
     const uint64_t b_ext = (uint64_t)(((K - 1) * ldb + N) * 2);
     if (rank == -1) {
         int64_t a_off;
@@ -499,6 +502,12 @@ gg_status gg_set_wait_limit_ns(uint64_t ns)
 }
 
 uint64_t gg_get_wait_limit_ns(void) { return g_wait_limit_ns.load(); }
+
+gg_status gg_debug_inject_stall(int enable)
+{
+    g_inject_stall.store(enable ? 1 : 0);
+    return ok();
+}
 
 const char *gg_last_error(void) { return g_last_error.c_str(); }
 

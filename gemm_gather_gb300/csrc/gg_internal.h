@@ -28,6 +28,7 @@ struct GatherArgs {
     int64_t tiles_n, tiles_per_src, total_items;
     int *status;
     uint64_t wait_limit_ns;
+    int inject_stall;  // test hook: program 0 never arms its first stage
 };
 
 // Bulk path: 16-byte aligned addresses, pitches, bn_b and row_b.
@@ -54,6 +55,7 @@ struct FusedArgs {
     int num_heaps;
     int *status;
     uint64_t wait_limit_ns;
+    int inject_stall;  // test hook: CTA 0 never arms its first ring stage
 };
 
 cudaError_t launch_matmul_all_gather(const FusedArgs &a, int programs, cudaStream_t s,

@@ -306,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                if (lane == 0) {
+                const bool stall = a.inject_stall && blockIdx.x == 0 && issued == 0;
+                if (lane == 0 && !stall) {  // test hook: the first stage is never armed
                     const uint32_t bar = ptx::smem_addr(&sh.full[stage]);
                     ptx::mbar_arrive_expect_tx(bar, kAStage + kBStage);
                     const uint32_t sa = base + kOffA + stage * kAStage;

@@ -204,6 +204,14 @@ gg_status gg_matmul_all_gather_check(const gg_heap *heap, int rank, const void *
 gg_status gg_set_wait_limit_ns(uint64_t ns);
 uint64_t gg_get_wait_limit_ns(void);
 
+/* Test hook for the bounded waits (failure detection without a GPU fault).
+ * While enabled, launches of the bulk all-gather path and of the fused
+ * kernel leave the first ring stage of program 0 unarmed, so the wait on it
+ * can never complete: it runs out after the wait limit, GG_ERR_TIMEOUT lands
+ * in the status word and the kernel drains and returns.  Nothing faults or
+ * hangs.  Off by default; 0 turns it off. */
+gg_status gg_debug_inject_stall(int enable);
+
 /* Message describing the last error returned on this thread ("" if none). */
 const char *gg_last_error(void);
 

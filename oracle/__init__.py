@@ -59,7 +59,7 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_encode16.restype = ctypes.c_uint16
     lib.oracle_matmul_f64.argtypes = [vp, i64, vp, i64, vp, i64, i64, i64, i64,
                                       i32, vp, i64]
-    lib.oracle_matmul_f64.restype = None
+    lib.oracle_matmul_f64.restype = i32
     lib.oracle_round16.argtypes = [vp, i64, vp, i64, i64, i64, i32]
     lib.oracle_round16.restype = None
     lib.oracle_set_threads.argtypes = [i32]
@@ -140,9 +140,11 @@ class Oracle:
         R = M if rows is None else len(rows)
         C = np.empty((R, N), dtype=np.float64)
         rows_arr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
-        self.lib.oracle_matmul_f64(A.ctypes.data, A.strides[0] // 2, B.ctypes.data,
-                                   B.strides[0] // 2, C.ctypes.data, N, M, N, K, fmt,
-                                   None if rows_arr is None else rows_arr.ctypes.data, R)
+        rc = self.lib.oracle_matmul_f64(A.ctypes.data, A.strides[0] // 2, B.ctypes.data,
+                                        B.strides[0] // 2, C.ctypes.data, N, M, N, K, fmt,
+                                        None if rows_arr is None else rows_arr.ctypes.data, R)
+        if rc:
+            raise MemoryError("oracle_matmul_f64: out of memory")
         return C
 
     def round16(self, C: np.ndarray, fmt: int) -> np.ndarray:

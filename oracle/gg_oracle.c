@@ -29,6 +29,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 /* ---------------------------------------------------------------------------
@@ -191,26 +192,53 @@ uint16_t oracle_encode16(double x, int fmt)
  * A: M x K, row pitch lda; B: K x N, row pitch ldb; both 16-bit (fmt);
  * C: M x N doubles, row pitch ldc.  C[m][n] = sum over k of A[m][k]*B[k][n],
  * each product and the sum in double precision, k ascending.
+ * The operands are decoded to double first (B into a transposed copy, so that
+ * each sum reads one contiguous row of it); the products and the order of
+ * the sum are exactly those of the definition.
  * Only the rows listed in `rows` (n_rows of them) are computed when rows is
  * non-NULL; row j of the result then holds row rows[j].
+ * Returns 0, or -1 if memory for the decoded operands is not available.
  * ------------------------------------------------------------------------- */
-void oracle_matmul_f64(const uint16_t *A, int64_t lda, const uint16_t *B,
-                       int64_t ldb, double *C, int64_t ldc, int64_t M,
-                       int64_t N, int64_t K, int fmt, const int64_t *rows,
-                       int64_t n_rows)
+int oracle_matmul_f64(const uint16_t *A, int64_t lda, const uint16_t *B,
+                      int64_t ldb, double *C, int64_t ldc, int64_t M,
+                      int64_t N, int64_t K, int fmt, const int64_t *rows,
+                      int64_t n_rows)
 {
     int64_t R = rows ? n_rows : M;
-#pragma omp parallel for schedule(dynamic, 1)
-    for (int64_t j = 0; j < R; ++j) {
-        int64_t m = rows ? rows[j] : j;
-        for (int64_t n = 0; n < N; ++n) {
-            double s = 0.0;
-            for (int64_t k = 0; k < K; ++k)
-                s += oracle_decode16(A[m * lda + k], fmt) *
-                     oracle_decode16(B[k * ldb + n], fmt);
-            C[j * ldc + n] = s;
+    double *bt = (double *)malloc(sizeof(double) * (size_t)(N * K > 0 ? N * K : 1));
+    if (!bt)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            bt[n * K + k] = oracle_decode16(B[k * ldb + n], fmt);
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *a = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        if (!a) {
+#pragma omp atomic write
+            failed = 1;
         }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t j = 0; j < R; ++j) {
+            if (!a)
+                continue;
+            int64_t m = rows ? rows[j] : j;
+            for (int64_t k = 0; k < K; ++k)
+                a[k] = oracle_decode16(A[m * lda + k], fmt);
+            for (int64_t n = 0; n < N; ++n) {
+                const double *b = bt + n * K;
+                double s = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    s += a[k] * b[k];
+                C[j * ldc + n] = s;
+            }
+        }
+        free(a);
     }
+    free(bt);
+    return failed ? -1 : 0;
 }
 
 /* Round an M x N block of doubles into 16-bit values (round to nearest even),

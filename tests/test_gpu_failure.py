@@ -1,8 +1,9 @@
-"""Bounded waits on the GPU: with the wait limit forced down to 1 ns, a wait
-inside each kernel gives up, the kernel stores GG_ERR_TIMEOUT in the status
-word, drains its copies in flight and returns; the context stays usable and a
-normal launch right after gives the oracle's result.  Nothing here faults,
-traps or hangs the GPU: the waits end on their own limit."""
+"""Bounded waits on the GPU.  With the stall hook on, program 0 of a launch
+leaves one ring stage unarmed, so the wait on it is a wait on a flag that
+nothing sets: it runs out after the (shortened) wait limit, the kernel stores
+GG_ERR_TIMEOUT in the status word, drains its copies in flight and returns.
+The context stays usable: a normal launch right after gives the oracle's
+result.  Nothing here faults, traps or hangs the GPU."""
 import numpy as np
 import pytest
 import torch
@@ -19,8 +20,10 @@ TIMEOUT = -6
 @pytest.fixture
 def short_waits():
     import gemm_gather_gb300 as gg
-    gg.set_wait_limit_ns(1)
+    gg.set_wait_limit_ns(20_000_000)
+    gg.debug_inject_stall(True)
     yield
+    gg.debug_inject_stall(False)
     gg.set_wait_limit_ns(0)  # back to the default
 
 
@@ -44,6 +47,7 @@ def test_gather_wait_limit_reports_timeout(oracle, short_waits):
     torch.cuda.synchronize()
     assert int(status.item()) == TIMEOUT
     # the context is intact: a normal launch gives the oracle's heap
+    gg.debug_inject_stall(False)
     gg.set_wait_limit_ns(0)
     status.zero_()
     gg.all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), lay.ld_in, sh.ptr(0, lay.out_off),
@@ -73,6 +77,7 @@ def test_fused_wait_limit_reports_timeout(oracle, short_waits):
                          M, N, K, torch.float16, gg.FUSED_TILE, 8, (0, 1, W), status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == TIMEOUT
+    gg.debug_inject_stall(False)
     gg.set_wait_limit_ns(0)
     status.zero_()
     gg.matmul_all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), K, Bd, N, sh.ptr(0, lay.out_off), N,

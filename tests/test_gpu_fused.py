@@ -49,7 +49,7 @@ def run_fused(oracle, H, group, M, N, K, dtype, programs, values="int", lda_pad=
     import gemm_gather_gb300 as gg
     start, stride, W = group
     members = [start + i * stride for i in range(W)]
-    lda = K + lda_pad
+    lda = (K + 7) // 8 * 8 + lda_pad  # TMA needs 16-byte row pitches
     lay = hi.make_layout(H, W, M, N, 2, ld_in=lda, ld_out=N + ld_out_pad)
     host = hi.sentinel_heap(lay)
     gen = gg_inputs.generator(seed)

@@ -22,8 +22,11 @@ MUTANTS = {
     "local_copy_skipped": ("for (int q = 0; q < world_size; ++q)", "for (int q = 1; q < world_size; ++q)"),
     "member_off_by_one": ("if (rank_start + i * rank_stride == h)", "if (rank_start + i * rank_stride == h + 1)"),
     "group_stride_ignored": ("int d = rank_start + q * rank_stride;", "int d = rank_start + q;"),
-    "dropped_first_k": ("for (int64_t k = 0; k < K; ++k)", "for (int64_t k = 1; k < K; ++k)"),
-    "wrong_sign_sum": ("s += oracle_decode16", "s -= oracle_decode16"),
+    "dropped_first_k": ("for (int64_t k = 0; k < K; ++k)\n                    s += a[k] * b[k];",
+                        "for (int64_t k = 1; k < K; ++k)\n                    s += a[k] * b[k];"),
+    "wrong_sign_sum": ("s += a[k] * b[k];", "s -= a[k] * b[k];"),
+    "b_transposed_pitch": ("bt[n * K + k] = oracle_decode16(B[k * ldb + n], fmt);",
+                           "bt[n * K + k] = oracle_decode16(B[(k % N) * ldb + (n % K)], fmt);"),
     "b_column_shifted": ("B[k * ldb + n]", "B[k * ldb + (n + 1) % N]"),
     "a_row_shifted": ("A[m * lda + k]", "A[((m + 1) % M) * lda + k]"),
     "decode_bias_off_by_one": ("v = ldexp((double)((1 << mbits) + f), e - bias - mbits);",
