@@ -21,12 +21,12 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
 import sys
 import time
+from dataclasses import dataclass, replace
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -34,26 +34,92 @@ sys.path.insert(0, ROOT)
 METRIC = "all-gather HBM GB/s & fused GEMM+gather TFLOP/s, % of roofline, 1xGB300"
 UNIT = "% of roofline"
 
-GATHER = dict(W=8, M=4096, N=4096, es=2, tile=(8, 256), programs=148)
-FUSED = dict(W=8, M=1024, N=3584, K=8192, tile=(128, 256))
+@dataclass
+class GatherCfg:
+    W: int = 8
+    M: int = 4096
+    N: int = 4096
+    dtype: str = "f16"
+    bm: int = 8
+    bn: int = 256
+    programs: int = 148
+    start: int = 0
+    stride: int = 1
+    values: str = "uniform"  # uniform[-1,1] or normal(0,1)
+    path: str = "auto"
+
+    @property
+    def es(self) -> int:
+        return ES[self.dtype]
+
+    def members(self):
+        return [self.start + i * self.stride for i in range(self.W)]
+
+    def describe(self) -> str:
+        grp = "" if (self.start, self.stride) == (0, 1) else \
+            f" group(start={self.start},stride={self.stride})"
+        return (f"all_gather W={self.W} {self.M}x{self.N} {self.dtype} tile {self.bm}x{self.bn} "
+                f"{self.programs} programs{grp}")
+
+
+@dataclass
+class FusedCfg:
+    W: int = 8
+    M: int = 1024
+    N: int = 3584
+    K: int = 8192
+    dtype: str = "f16"
+    programs: int = 0  # 0: one CTA per SM
+    start: int = 0
+    stride: int = 1
+
+    def members(self):
+        return [self.start + i * self.stride for i in range(self.W)]
+
+    def describe(self) -> str:
+        grp = "" if (self.start, self.stride) == (0, 1) else \
+            f" group(start={self.start},stride={self.stride})"
+        return (f"matmul_all_gather W={self.W} M_local={self.M} N={self.N} K={self.K} "
+                f"{self.dtype} tile 128x256{grp}")
+
+
+ES = {"f16": 2, "bf16": 2, "f32": 4}
+GATHER = GatherCfg()
+FUSED = FusedCfg()
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 F16_PER_BF16 = 1.0  # nominal dense f16 : bf16 tensor rate
 
 
-def gather_bytes(c=GATHER) -> float:
+def parse_cfg(text: str, base):
+    """'W=8,M=4096,tile=8x256,group=1:2,...' -> a copy of `base` with those fields."""
+    cfg = replace(base)
+    for item in filter(None, text.split(",")):
+        k, v = item.split("=")
+        if k == "tile":
+            cfg.bm, cfg.bn = (int(x) for x in v.split("x"))
+        elif k == "group":
+            cfg.start, cfg.stride = (int(x) for x in v.split(":"))
+        elif k in ("dtype", "values", "path"):
+            setattr(cfg, k, v)
+        else:
+            setattr(cfg, k, int(v))
+    return cfg
+
+
+def gather_bytes(c: GatherCfg) -> float:
     """Algorithmic bytes: every rank's block read once, W copies of W blocks written."""
-    blk = c["M"] * c["N"] * c["es"]
-    return c["W"] * blk + c["W"] * c["W"] * blk
+    blk = c.M * c.N * c.es
+    return c.W * blk + c.W * c.W * blk
 
 
-def fused_flops(c=FUSED) -> float:
-    return 2.0 * c["W"] * c["M"] * c["N"] * c["K"]
+def fused_flops(c: FusedCfg) -> float:
+    return 2.0 * c.W * c.M * c.N * c.K
 
 
-def fused_bytes(c=FUSED) -> float:
+def fused_bytes(c: FusedCfg) -> float:
     """A of every rank + B once + W copies of every rank's C block."""
-    return 2.0 * (c["W"] * c["M"] * c["K"] + c["K"] * c["N"] + c["W"] ** 2 * c["M"] * c["N"])
+    return 2.0 * (c.W * c.M * c.K + c.K * c.N + c.W ** 2 * c.M * c.N)
 
 
 def load_peaks():
@@ -65,11 +131,11 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def roofline_times(peaks):
+def roofline_times(peaks, g: GatherCfg | None, f: FusedCfg | None):
     hbm = peaks["hbm_gbs"] * 1e9
     tc = peaks["bf16_tflops"] * 1e12 * F16_PER_BF16
-    t_g = gather_bytes() / hbm
-    t_f = max(fused_flops() / tc, fused_bytes() / hbm)
+    t_g = gather_bytes(g) / hbm if g else 0.0
+    t_f = max(fused_flops(f) / tc, fused_bytes(f) / hbm) if f else 0.0
     return t_g, t_f
 
 
@@ -149,66 +215,79 @@ class ClockSampler:
 # CPU oracle on a bounded sample (reference arm and cpu_baseline)             #
 # --------------------------------------------------------------------------- #
 
-def oracle_sample_step(orc, gather_rows: int, fused_rows: int, seed: int = 0):
-    """One sampled step of the oracle: the gather on `gather_rows` of the
-    4096 rows per rank, the fused path on `fused_rows` of the 1024 rows per
-    rank (all N columns, full K).  Returns (gather seconds, fused seconds)."""
+def oracle_sample_step(orc, g: GatherCfg | None, f: FusedCfg | None, gather_rows: int,
+                       fused_rows: int, seed: int = 0):
+    """One sampled step of the oracle: the gather on `gather_rows` of the M
+    rows per rank, the fused path on `fused_rows` of the M rows per rank (all
+    N columns, full K).  Returns (gather seconds, fused seconds)."""
     import numpy as np
     import torch
 
     import gg_inputs
-    g, f = GATHER, FUSED
-    W = g["W"]
     gen = gg_inputs.generator(seed)
-    # gather sample heap: input block + gathered output per partition
-    blk = gather_rows * g["N"] * 2
-    part = blk + W * blk
-    heap = np.full(W * part, gg_inputs.SENTINEL_BYTE, dtype=np.uint8)
-    for h in range(W):
-        x = gg_inputs.uniform_pm1((gather_rows, g["N"]), torch.float16, gen)
-        heap[h * part: h * part + blk] = x.view(torch.int16).numpy().view(np.uint8).ravel()
-    # fused sample heap: A rows + gathered output per partition
-    a_bytes = fused_rows * f["K"] * 2
-    c_bytes = W * fused_rows * f["N"] * 2
-    fpart = a_bytes + c_bytes
-    fheap = np.zeros(W * fpart, dtype=np.uint8)
-    for h in range(W):
-        a = gg_inputs.normal((fused_rows, f["K"]), torch.float16, gen, scale=f["K"] ** -0.5)
-        fheap[h * fpart: h * fpart + a_bytes] = a.view(torch.int16).numpy().view(np.uint8).ravel()
-    B = gg_inputs.normal((f["K"], f["N"]), torch.float16, gen, scale=f["K"] ** -0.5)
-    Bb = B.view(torch.int16).numpy().view(np.uint16)
-    t0 = time.perf_counter()
-    orc.all_gather(heap, part, 0, g["N"], blk, g["N"], gather_rows, g["N"], 2, (0, 1, W))
-    t1 = time.perf_counter()
-    orc.matmul_all_gather(fheap, fpart, 0, f["K"], Bb, a_bytes, f["N"], fused_rows, f["N"],
-                          f["K"], 0, (0, 1, W))
-    t2 = time.perf_counter()
-    return t1 - t0, t2 - t1
+    t_g = t_f = 0.0
+    if g is not None:
+        W, es = g.W, g.es
+        dt = gg_inputs.DTYPES[g.dtype]
+        blk = gather_rows * g.N * es
+        part = blk + W * blk
+        H = g.members()[-1] + 1
+        heap = np.full(H * part, gg_inputs.SENTINEL_BYTE, dtype=np.uint8)
+        for h in g.members():
+            x = (gg_inputs.uniform_pm1 if g.values == "uniform" else gg_inputs.normal)(
+                (gather_rows, g.N), dt, gen)
+            heap[h * part: h * part + blk] = x.contiguous().view(torch.uint8).numpy().ravel()
+        t0 = time.perf_counter()
+        orc.all_gather(heap, part, 0, g.N, blk, g.N, gather_rows, g.N, es,
+                       (g.start, g.stride, W))
+        t_g = time.perf_counter() - t0
+    if f is not None:
+        W = f.W
+        dt = gg_inputs.DTYPES[f.dtype]
+        a_bytes = fused_rows * f.K * 2
+        fpart = a_bytes + W * fused_rows * f.N * 2
+        H = f.members()[-1] + 1
+        fheap = np.zeros(H * fpart, dtype=np.uint8)
+        for h in f.members():
+            a = gg_inputs.normal((fused_rows, f.K), dt, gen, scale=f.K ** -0.5)
+            fheap[h * fpart: h * fpart + a_bytes] = a.view(torch.uint8).numpy().ravel()
+        B = gg_inputs.normal((f.K, f.N), dt, gen, scale=f.K ** -0.5)
+        Bb = B.view(torch.int16).numpy().view(np.uint16)
+        t0 = time.perf_counter()
+        orc.matmul_all_gather(fheap, fpart, 0, f.K, Bb, a_bytes, f.N, fused_rows, f.N, f.K,
+                              0 if f.dtype == "f16" else 1, (f.start, f.stride, W))
+        t_f = time.perf_counter() - t0
+    return t_g, t_f
 
 
-def size_sample(orc, seconds: float):
+def size_sample(orc, g, f, seconds: float):
     """Rows of the gather and of the fused path whose oracle run takes about
-    `seconds` (30% gather, 70% fused), from a small calibration run."""
+    `seconds` (30% gather, 70% fused when both run), from a small calibration."""
     cg, cf = 16, 4
-    t_g, t_f = oracle_sample_step(orc, cg, cf)
-    rows_g = int(max(8, min(GATHER["M"], cg * 0.3 * seconds / max(t_g, 1e-6))))
-    rows_f = int(max(1, min(FUSED["M"], cf * 0.7 * seconds / max(t_f, 1e-6))))
+    t_g, t_f = oracle_sample_step(orc, g, f, cg, cf)
+    share_g = 0.3 if (g and f) else 1.0
+    rows_g = int(max(8, min(g.M, cg * share_g * seconds / max(t_g, 1e-6)))) if g else 0
+    rows_f = int(max(1, min(f.M, cf * (1 - share_g if g else 1.0) * seconds
+                            / max(t_f, 1e-6)))) if f else 0
     return rows_g, rows_f
 
 
-def cpu_baseline(peaks, budget_s: float = 15.0):
+def cpu_baseline(peaks, g, f, budget_s: float = 15.0):
     import oracle
     orc = oracle.Oracle()
     cores = orc.max_threads()
-    t_rg, t_rf = roofline_times(peaks)
-    rows_g, rows_f = size_sample(orc, budget_s)
-    t_g, t_f = oracle_sample_step(orc, rows_g, rows_f)
-    t_full = t_g * GATHER["M"] / rows_g + t_f * FUSED["M"] / rows_f
+    t_rg, t_rf = roofline_times(peaks, g, f)
+    rows_g, rows_f = size_sample(orc, g, f, budget_s)
+    t_g, t_f = oracle_sample_step(orc, g, f, rows_g, rows_f)
+    t_full = (t_g * g.M / rows_g if g else 0.0) + (t_f * f.M / rows_f if f else 0.0)
     value = 100.0 * (t_rg + t_rf) / t_full
+    parts = []
+    if g:
+        parts.append(f"gather on {rows_g} of {g.M} rows per rank ({t_g:.2f} s)")
+    if f:
+        parts.append(f"fused path on {rows_f} of {f.M} rows per rank, full K and N ({t_f:.2f} s)")
     return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": (f"gather on {rows_g} of 4096 rows per rank ({t_g:.2f} s) and fused path "
-                       f"on {rows_f} of 1024 rows per rank, full K and N ({t_f:.2f} s); "
-                       f"scaled by rows to a full step: {t_full:.1f} s/step"),
+            "sample": " and ".join(parts) + f"; scaled by rows to a full step: {t_full:.1f} s/step",
             "seconds_per_step": t_full}
 
 
@@ -216,94 +295,197 @@ def cpu_baseline(peaks, budget_s: float = 15.0):
 # reference arm                                                               #
 # --------------------------------------------------------------------------- #
 
-def run_reference(args, peaks, peak_src):
+def run_reference(args, peaks, peak_src, g, f):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     import oracle
     orc = oracle.Oracle()
     cores = orc.max_threads()
-    t_rg, t_rf = roofline_times(peaks)
+    t_rg, t_rf = roofline_times(peaks, g, f)
     # size each step's sample so warmup + steps finish in about two minutes
-    rows_g, rows_f = size_sample(orc, 120.0 / max(1, args.steps + args.warmup))
+    rows_g, rows_f = size_sample(orc, g, f, 120.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle_sample_step(orc, rows_g, rows_f)
+        oracle_sample_step(orc, g, f, rows_g, rows_f)
     total = 0.0
     for _ in range(args.steps):
-        t_g, t_f = oracle_sample_step(orc, rows_g, rows_f)
+        t_g, t_f = oracle_sample_step(orc, g, f, rows_g, rows_f)
         total += t_g + t_f
     # the sampled step holds this share of the full step's roofline time
-    sample_roof = t_rg * (rows_g / GATHER["M"]) + t_rf * (rows_f / FUSED["M"])
+    sample_roof = (t_rg * rows_g / g.M if g else 0.0) + (t_rf * rows_f / f.M if f else 0.0)
     value = 100.0 * sample_roof / (total / args.steps)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": config_block(peaks, peak_src),
+        "config": config_block(peaks, peak_src, g, f),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": (f"each step: oracle gather on {rows_g} of 4096 rows per rank "
-                                    f"and fused path on {rows_f} of 1024 rows per rank")},
+                         "sample": (f"each step: oracle gather on {rows_g} rows per rank and "
+                                    f"fused path on {rows_f} rows per rank")},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
     return 0
 
 
-def config_block(peaks, peak_src):
-    return {
-        "workload": ("all_gather W=8 4096x4096 f16 tile 8x256 148 programs + "
-                     "matmul_all_gather W=8 M_local=1024 N=3584 K=8192 f16 tile 128x256"),
-        "all_gather": {"W": 8, "M_local": 4096, "N": 4096, "dtype": "f16", "tile": [8, 256],
-                       "comm_programs": GATHER["programs"], "values": "uniform[-1,1]"},
-        "matmul_all_gather": {"W": 8, "M_local": 1024, "N": 3584, "K": 8192, "dtype": "f16",
-                              "tile": [128, 256], "values": "normal(0,1)/sqrt(K)"},
-        "l2": "inputs larger than L2 (about 3 GB touched per step)",
-        "peaks": {"hbm_gbs": peaks["hbm_gbs"], "f16_tflops": peaks["bf16_tflops"] * F16_PER_BF16,
-                  "source": peak_src,
-                  "note": "f16 dense peak = measured bf16 burst peak x nominal 1:1 ratio"},
-        "seed": 0,
-    }
+def config_block(peaks, peak_src, g, f):
+    work = " + ".join(c.describe() for c in (g, f) if c is not None)
+    touched = (gather_bytes(g) if g else 0) + (fused_bytes(f) if f else 0)
+    cfg = {"workload": work}
+    if g:
+        cfg["all_gather"] = {"W": g.W, "M_local": g.M, "N": g.N, "dtype": g.dtype,
+                             "tile": [g.bm, g.bn], "comm_programs": g.programs,
+                             "group": [g.start, g.stride, g.W], "path": g.path,
+                             "values": "uniform[-1,1]" if g.values == "uniform" else "normal(0,1)"}
+    if f:
+        cfg["matmul_all_gather"] = {"W": f.W, "M_local": f.M, "N": f.N, "K": f.K,
+                                    "dtype": f.dtype, "tile": [128, 256],
+                                    "group": [f.start, f.stride, f.W],
+                                    "values": "normal(0,1)/sqrt(K)"}
+    cfg["l2"] = (f"inputs larger than L2 ({touched / 1e9:.2f} GB of algorithmic traffic per step)"
+                 if touched > 2 * 126e6 else
+                 f"small case: {touched / 1e6:.0f} MB per step, partly L2-resident")
+    cfg["peaks"] = {"hbm_gbs": peaks["hbm_gbs"],
+                    "f16_tflops": peaks["bf16_tflops"] * F16_PER_BF16, "source": peak_src,
+                    "note": "f16 dense peak = measured bf16 burst peak x nominal 1:1 ratio"}
+    cfg["seed"] = 0
+    return cfg
 
 
 # --------------------------------------------------------------------------- #
 # the GPU arm                                                                 #
 # --------------------------------------------------------------------------- #
 
-def setup_device(dev, seed=0):
+def setup_device(dev, g: GatherCfg | None, f: FusedCfg | None, device_inputs: bool, seed=0):
+    """One symmetric heap holding every member's inputs and outputs; returns
+    (heap, offsets, B on the device, host copies of the inputs or None)."""
     import torch
 
     import gemm_gather_gb300 as gg
     import gg_inputs
-    g, f = GATHER, FUSED
-    W = g["W"]
-    gin = g["M"] * g["N"] * 2
-    gout = W * gin
-    fa = f["M"] * f["K"] * 2
-    fout = W * f["M"] * f["N"] * 2
     align = 1 << 16
-    offs = {}
-    o = 0
-    for name, size in (("g_in", gin), ("g_out", gout), ("f_a", fa), ("f_out", fout)):
+    sizes = []
+    if g:
+        sizes += [("g_in", g.M * g.N * g.es), ("g_out", g.W * g.M * g.N * g.es)]
+    if f:
+        sizes += [("f_a", f.M * f.K * 2), ("f_out", f.W * f.M * f.N * 2)]
+    offs, o = {}, 0
+    for name, size in sizes:
         offs[name] = o
         o += (size + align - 1) // align * align
-    part = o
-    sh = gg.SymmetricHeap(W, part, device=dev)
-    gen = gg_inputs.generator(seed)
-    host = {"g_in": [], "f_a": []}
-    for h in range(W):
-        x = gg_inputs.uniform_pm1((g["M"], g["N"]), torch.float16, gen)
-        host["g_in"].append(x)
-        sh.view(h, offs["g_in"], g["M"], g["N"], g["N"], torch.float16).copy_(x.to(dev))
-    for h in range(W):
-        a = gg_inputs.normal((f["M"], f["K"]), torch.float16, gen, scale=f["K"] ** -0.5)
-        host["f_a"].append(a)
-        sh.view(h, offs["f_a"], f["M"], f["K"], f["K"], torch.float16).copy_(a.to(dev))
-    B = gg_inputs.normal((f["K"], f["N"]), torch.float16, gen, scale=f["K"] ** -0.5)
-    host["B"] = B
-    Bd = B.to(dev)
+    H = max((c.members()[-1] + 1) for c in (g, f) if c is not None)
+    sh = gg.SymmetricHeap(H, o, device=dev)
+    gen = gg_inputs.generator(seed, device=dev if device_inputs else "cpu")
+    host = None if device_inputs else {"g_in": {}, "f_a": {}}
+    if g:
+        dt = gg_inputs.DTYPES[g.dtype]
+        draw = gg_inputs.uniform_pm1 if g.values == "uniform" else gg_inputs.normal
+        for h in g.members():
+            x = draw((g.M, g.N), dt, gen)
+            if host is not None:
+                host["g_in"][h] = x
+            sh.view(h, offs["g_in"], g.M, g.N, g.N, dt).copy_(x)
+    Bd = None
+    if f:
+        dt = gg_inputs.DTYPES[f.dtype]
+        for h in f.members():
+            a = gg_inputs.normal((f.M, f.K), dt, gen, scale=f.K ** -0.5)
+            if host is not None:
+                host["f_a"][h] = a
+            sh.view(h, offs["f_a"], f.M, f.K, f.K, dt).copy_(a)
+        B = gg_inputs.normal((f.K, f.N), dt, gen, scale=f.K ** -0.5)
+        if host is not None:
+            host["B"] = B
+        Bd = B.to(dev)
     torch.cuda.synchronize(dev)
     return sh, offs, Bd, host
+
+
+def sweep_points(name: str):
+    """(GatherCfg | None, FusedCfg | None) points of the configuration sweeps."""
+    pts = []
+    if name == "budget":  # 8 ranks, 4096x4096 f16, tile 8x256, budget swept
+        for p in (8, 16, 32, 64, 148):
+            pts.append((replace(GATHER, programs=p), None))
+    elif name == "gather":  # 4 and 8 ranks, M x N x dtype x tile x budget, normal values
+        for W in (4, 8):
+            for M in (1024, 4096, 16384):
+                for N in (4096, 8192):
+                    for dt in ("f16", "bf16", "f32"):
+                        for bm, bn in ((8, 256), (16, 128), (32, 128)):
+                            for p in (64, 128, 148):
+                                pts.append((GatherCfg(W=W, M=M, N=N, dtype=dt, bm=bm, bn=bn,
+                                                      programs=p, values="normal"), None))
+        for M in (1024, 4096, 16384):  # strided subgroup: heaps 1, 3, 5, 7
+            for N in (4096, 8192):
+                pts.append((GatherCfg(W=4, M=M, N=N, dtype="f16", start=1, stride=2,
+                                      values="normal"), None))
+    elif name == "fused":  # 8 ranks, M_local 1024/4096/16384, f16 and bf16, + subgroup (0,2,4)
+        for M in (1024, 4096, 16384):
+            for dt in ("f16", "bf16"):
+                pts.append((None, replace(FUSED, M=M, dtype=dt)))
+        for M in (4096, 16384):
+            for dt in ("f16", "bf16"):
+                pts.append((None, replace(FUSED, M=M, dtype=dt, W=4, start=0, stride=2)))
+    else:
+        raise SystemExit(f"unknown sweep {name}")
+    return pts
+
+
+def run_sweep(args):
+    """Time each point of a sweep in this process; one JSON line per point."""
+    import torch
+
+    import gemm_gather_gb300 as gg
+    import gg_inputs
+    peaks, peak_src = load_peaks()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    for g, f in sweep_points(args.sweep):
+        if f and f.programs == 0:
+            f.programs = sms
+        sh, offs, Bd, _ = setup_device(dev, g, f, device_inputs=True)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def launch():
+            if g:
+                gg.all_gather(sh.heap, -1, sh.ptr(g.start, offs["g_in"]), g.N,
+                              sh.ptr(g.start, offs["g_out"]), g.N, g.M, g.N,
+                              gg_inputs.DTYPES[g.dtype], (g.bm, g.bn), g.programs,
+                              (g.start, g.stride, g.W), status=status, path=g.path)
+            else:
+                gg.matmul_all_gather(sh.heap, -1, sh.ptr(f.start, offs["f_a"]), f.K, Bd, f.N,
+                                     sh.ptr(f.start, offs["f_out"]), f.N, f.M, f.N, f.K,
+                                     gg_inputs.DTYPES[f.dtype], gg.FUSED_TILE, f.programs,
+                                     (f.start, f.stride, f.W), status=status)
+
+        t_rg, t_rf = roofline_times(peaks, g, f)
+        work = t_rg + t_rf
+        steps = int(max(5, min(args.steps, 0.5 / max(work, 1e-6))))
+        for _ in range(args.warmup):
+            launch()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            launch()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())}")
+        rec = {"sweep": args.sweep, "workload": (g or f).describe(), "ms": ms, "steps": steps,
+               "roofline_ms": 1e3 * work, "frac": 1e3 * work / ms}
+        if g:
+            rec["GB/s"] = gather_bytes(g) / (ms * 1e-3) / 1e9
+        else:
+            rec["TFLOP/s"] = fused_flops(f) / (ms * 1e-3) / 1e12
+        print(json.dumps(rec), flush=True)
+        del sh, Bd, status
+        torch.cuda.empty_cache()
+    return 0
 
 
 def main():
@@ -312,21 +494,33 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--workload", default="step", choices=["step", "gather", "fused"],
+                    help="step: the all-gather then the fused kernel; or one of them alone")
+    ap.add_argument("--gather", default="", help="overrides, e.g. W=4,M=1024,N=8192,dtype=f32,"
+                    "tile=16x128,programs=128,group=1:2,values=normal,path=bulk")
+    ap.add_argument("--fused", default="", help="overrides, e.g. M=16384,dtype=bf16,group=0:2,W=4")
+    ap.add_argument("--e2e-steps", type=int, default=20, help="0 skips the end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--gather-path", default="auto", choices=["auto", "bulk", "vector"])
-    ap.add_argument("--fused-programs", type=int, default=0, help="0: one CTA per SM")
+    ap.add_argument("--device-inputs", default="auto", choices=["auto", "yes", "no"],
+                    help="draw inputs on the GPU (seeded) instead of the CPU")
     ap.add_argument("--clocks-out", default=None)
+    ap.add_argument("--sweep", default=None, choices=["budget", "gather", "fused"],
+                    help="time every point of a configuration sweep (one JSON line each)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.sweep:
+        return run_sweep(args)
+    g = parse_cfg(args.gather, GATHER) if args.workload in ("step", "gather") else None
+    f = parse_cfg(args.fused, FUSED) if args.workload in ("step", "fused") else None
     peaks, peak_src = load_peaks()
     if args.impl == "reference":
-        return run_reference(args, peaks, peak_src)
+        return run_reference(args, peaks, peak_src, g, f)
 
     import torch
     import torch.distributed as dist
 
     import gemm_gather_gb300 as gg
+    import gg_inputs
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -336,26 +530,32 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    fused_programs = args.fused_programs or sms
-    g, f = GATHER, FUSED
-    W = g["W"]
-    group = (0, 1, W)
-    sh, offs, Bd, host = setup_device(dev)
+    if f and f.programs == 0:
+        f.programs = sms
+    in_bytes = (g.W * g.M * g.N * g.es if g else 0) + (f.W * f.M * f.K * 2 if f else 0)
+    device_inputs = args.device_inputs == "yes" or (args.device_inputs == "auto"
+                                                   and in_bytes > (1 << 30))
+    sh, offs, Bd, host = setup_device(dev, g, f, device_inputs)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    gdt = gg_inputs.DTYPES[g.dtype] if g else None
+    fdt = gg_inputs.DTYPES[f.dtype] if f else None
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        gg.all_gather(sh.heap, -1, sh.ptr(0, offs["g_in"]), g["N"], sh.ptr(0, offs["g_out"]),
-                      g["N"], g["M"], g["N"], torch.float16, g["tile"], g["programs"], group,
-                      status=status, stream=stream, path=args.gather_path)
+        if g:
+            gg.all_gather(sh.heap, -1, sh.ptr(g.start, offs["g_in"]), g.N,
+                          sh.ptr(g.start, offs["g_out"]), g.N, g.M, g.N, gdt, (g.bm, g.bn),
+                          g.programs, (g.start, g.stride, g.W), status=status, stream=stream,
+                          path=g.path)
         if ev is not None:
             ev[1].record(stream)
-        gg.matmul_all_gather(sh.heap, -1, sh.ptr(0, offs["f_a"]), f["K"], Bd, f["N"],
-                             sh.ptr(0, offs["f_out"]), f["N"], f["M"], f["N"], f["K"],
-                             torch.float16, f["tile"], fused_programs, group, status=status,
-                             stream=stream)
+        if f:
+            gg.matmul_all_gather(sh.heap, -1, sh.ptr(f.start, offs["f_a"]), f.K, Bd, f.N,
+                                 sh.ptr(f.start, offs["f_out"]), f.N, f.M, f.N, f.K, fdt,
+                                 gg.FUSED_TILE, f.programs, (f.start, f.stride, f.W),
+                                 status=status, stream=stream)
         if ev is not None:
             ev[2].record(stream)
 
@@ -374,21 +574,17 @@ def main():
     barrier()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    if clocks:
-        clocks.mark(True)
     t_start.record(stream)
     for i in range(args.steps):
         step(evs[i])
     t_end.record(stream)
     barrier()
-    if clocks:
-        clocks.mark(False)
     clk = clocks.stop() if clocks else None
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} after the timed steps")
     elapsed_ms = t_start.elapsed_time(t_end)
-    g_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    f_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    g_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) if g else 0.0
+    f_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) if f else 0.0
     if world > 1:
         t = torch.tensor([elapsed_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -396,93 +592,115 @@ def main():
     ms_step = elapsed_ms / args.steps
 
     # ---- end to end through the C ABI, host buffers, copies in the timed region
-    pinned_in = [x.pin_memory() for x in host["g_in"]]
-    pinned_a = [x.pin_memory() for x in host["f_a"]]
-    pinned_b = host["B"].pin_memory()
-    out_g = torch.empty((W, W * g["M"], g["N"]), dtype=torch.float16).pin_memory()
-    out_f = torch.empty((W, W * f["M"], f["N"]), dtype=torch.float16).pin_memory()
-    h2d = sum(x.numel() * 2 for x in pinned_in) + sum(x.numel() * 2 for x in pinned_a) \
-        + pinned_b.numel() * 2
-    d2h = out_g.numel() * 2 + out_f.numel() * 2
+    e2e = None
+    if args.e2e_steps > 0:
+        if host is None:  # inputs were drawn on the device: stage them to the host once
+            host = {"g_in": {}, "f_a": {}}
+            if g:
+                for h in g.members():
+                    host["g_in"][h] = sh.view(h, offs["g_in"], g.M, g.N, g.N, gdt).cpu()
+            if f:
+                for h in f.members():
+                    host["f_a"][h] = sh.view(h, offs["f_a"], f.M, f.K, f.K, fdt).cpu()
+                host["B"] = Bd.cpu()
+        pin = {k: {h: x.pin_memory() for h, x in v.items()} for k, v in host.items() if k != "B"}
+        pin_b = host["B"].pin_memory() if f else None
+        out_g = {h: torch.empty((g.W * g.M, g.N), dtype=gdt).pin_memory()
+                 for h in g.members()} if g else {}
+        out_f = {h: torch.empty((f.W * f.M, f.N), dtype=fdt).pin_memory()
+                 for h in f.members()} if f else {}
+        h2d = sum(x.numel() * x.element_size() for v in pin.values() for x in v.values()) + \
+            (pin_b.numel() * 2 if f else 0)
+        d2h = sum(x.numel() * x.element_size() for x in list(out_g.values()) + list(out_f.values()))
 
-    def e2e_step():
-        for h in range(W):
-            sh.view(h, offs["g_in"], g["M"], g["N"], g["N"], torch.float16).copy_(
-                pinned_in[h], non_blocking=True)
-            sh.view(h, offs["f_a"], f["M"], f["K"], f["K"], torch.float16).copy_(
-                pinned_a[h], non_blocking=True)
-        Bd.copy_(pinned_b, non_blocking=True)
-        step()
-        for h in range(W):
-            out_g[h].copy_(sh.view(h, offs["g_out"], W * g["M"], g["N"], g["N"], torch.float16),
-                           non_blocking=True)
-            out_f[h].copy_(sh.view(h, offs["f_out"], W * f["M"], f["N"], f["N"], torch.float16),
-                           non_blocking=True)
+        def e2e_step():
+            if g:
+                for h in g.members():
+                    sh.view(h, offs["g_in"], g.M, g.N, g.N, gdt).copy_(pin["g_in"][h],
+                                                                        non_blocking=True)
+            if f:
+                for h in f.members():
+                    sh.view(h, offs["f_a"], f.M, f.K, f.K, fdt).copy_(pin["f_a"][h],
+                                                                       non_blocking=True)
+                Bd.copy_(pin_b, non_blocking=True)
+            step()
+            for h, o in out_g.items():
+                o.copy_(sh.view(h, offs["g_out"], g.W * g.M, g.N, g.N, gdt), non_blocking=True)
+            for h, o in out_f.items():
+                o.copy_(sh.view(h, offs["f_out"], f.W * f.M, f.N, f.N, fdt), non_blocking=True)
 
-    e2e_steps = max(1, min(args.e2e_steps, args.steps))
-    for _ in range(3):
-        e2e_step()
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    barrier()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+        e2e_steps = max(1, min(args.e2e_steps, args.steps))
+        for _ in range(3):
+            e2e_step()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "steps": e2e_steps,
+               "path": "pinned host -> heap (cudaMemcpyAsync) -> C-ABI calls -> pinned host"}
 
     # ---- roofline bookkeeping
-    t_rg, t_rf = roofline_times(peaks)
+    t_rg, t_rf = roofline_times(peaks, g, f)
     roof_step = t_rg + t_rf
     value = 100.0 * world * roof_step / (ms_step * 1e-3)
-    e2e_value = 100.0 * world * roof_step / (e2e_ms * 1e-3)
-    g_gbs = gather_bytes() / (g_ms * 1e-3) / 1e9
-    f_tfs = fused_flops() / (f_ms * 1e-3) / 1e12
+    if e2e:
+        e2e = {"value": 100.0 * world * roof_step / (e2e["ms_per_step"] * 1e-3), "unit": UNIT,
+               **e2e}
     hbm_peak = peaks["hbm_gbs"]
     tc_peak = peaks["bf16_tflops"] * F16_PER_BF16
-    kernels = {
-        "all_gather": {"kernel": "ag_bulk_kernel" if args.gather_path != "vector" else "ag_vec_kernel",
-                       "ms": g_ms, "GB/s": g_gbs, "roofline_ms": 1e3 * t_rg,
-                       "frac": g_gbs / hbm_peak, "bound": "hbm",
-                       "algorithmic_bytes": gather_bytes()},
-        "matmul_all_gather": {"kernel": "mag_kernel", "ms": f_ms, "TFLOP/s": f_tfs,
-                              "roofline_ms": 1e3 * t_rf, "frac": f_tfs / tc_peak,
-                              "bound": "tensor", "algorithmic_flops": fused_flops(),
-                              "programs": fused_programs},
-    }
-    if g_ms >= f_ms:
-        roof = {"kernel": "ag_bulk_kernel", "bound": "hbm", "achieved": g_gbs, "peak": hbm_peak,
-                "unit": "GB/s", "frac": g_gbs / hbm_peak,
-                "traffic": traffic_for("ag_bulk_kernel", "ag_kernels.cu"),
+    kernels = {}
+    if g:
+        g_gbs = gather_bytes(g) / (g_ms * 1e-3) / 1e9
+        kname = "ag_vec_kernel" if g.path == "vector" else "ag_bulk_kernel"
+        kernels["all_gather"] = {"kernel": kname, "ms": g_ms, "GB/s": g_gbs,
+                                 "roofline_ms": 1e3 * t_rg, "frac": g_gbs / hbm_peak,
+                                 "bound": "hbm", "algorithmic_bytes": gather_bytes(g)}
+    if f:
+        f_tfs = fused_flops(f) / (f_ms * 1e-3) / 1e12
+        kernels["matmul_all_gather"] = {"kernel": "mag_kernel", "ms": f_ms, "TFLOP/s": f_tfs,
+                                        "roofline_ms": 1e3 * t_rf, "frac": f_tfs / tc_peak,
+                                        "bound": "tensor", "algorithmic_flops": fused_flops(f),
+                                        "programs": f.programs}
+    if g and (not f or g_ms >= f_ms):
+        k = kernels["all_gather"]
+        roof = {"kernel": k["kernel"], "bound": "hbm", "achieved": k["GB/s"], "peak": hbm_peak,
+                "unit": "GB/s", "frac": k["frac"],
+                "traffic": traffic_for(k["kernel"], "ag_kernels.cu"),
                 "per_unit": "bytes = W*M*N*s reads + W^2*M*N*s writes per launch"}
     else:
-        roof = {"kernel": "mag_kernel", "bound": "tensor", "achieved": f_tfs, "peak": tc_peak,
-                "unit": "TFLOP/s", "frac": f_tfs / tc_peak,
+        k = kernels["matmul_all_gather"]
+        roof = {"kernel": "mag_kernel", "bound": "tensor", "achieved": k["TFLOP/s"],
+                "peak": tc_peak, "unit": "TFLOP/s", "frac": k["frac"],
                 "traffic": traffic_for("mag_kernel", "mag_kernel.cu"),
                 "per_unit": "FLOPs = 2*W*M*N*K per launch"}
-    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else peak_src
+    roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peak_src == "measured"
+                           else "fallback")
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return 0
-    cpu = None if args.no_cpu_baseline else cpu_baseline(peaks)
+    cpu = None if args.no_cpu_baseline else cpu_baseline(peaks, g, f)
+    dtypes = sorted({c.dtype for c in (g, f) if c is not None})
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": config_block(peaks, peak_src),
+        "scaling": "weak", "vs_baseline": None, "dtype": "+".join(dtypes), "data": "synthetic",
+        "config": config_block(peaks, peak_src, g, f),
         "kernels": kernels,
         "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": e2e_steps,
-                "path": "pinned host -> heap (cudaMemcpyAsync) -> C-ABI calls -> pinned host"},
-        "gpu_launches": 2 * args.steps,
+        "e2e": e2e,
+        "gpu_launches": (int(g is not None) + int(f is not None)) * args.steps,
         "clocks": clk,
         "device": torch.cuda.get_device_name(dev), "sms": sms,
         "torch": torch.__version__,

@@ -25,24 +25,27 @@ DTYPES = {
 }
 
 
-def generator(seed: int = 0) -> torch.Generator:
-    g = torch.Generator(device="cpu")
+def generator(seed: int = 0, device="cpu") -> torch.Generator:
+    """Seeded generator; on the CPU unless a device is named (benchmarks of
+    large shapes draw on the GPU; parity tests always draw on the CPU)."""
+    g = torch.Generator(device=device)
     g.manual_seed(seed)
     return g
 
 
 def uniform_pm1(shape, dtype: torch.dtype, gen: torch.Generator) -> torch.Tensor:
-    u = torch.rand(shape, generator=gen, dtype=torch.float32)
+    u = torch.rand(shape, generator=gen, dtype=torch.float32, device=gen.device)
     return (2.0 * u - 1.0).to(dtype)
 
 
 def normal(shape, dtype: torch.dtype, gen: torch.Generator, scale: float = 1.0) -> torch.Tensor:
-    x = torch.randn(shape, generator=gen, dtype=torch.float32)
+    x = torch.randn(shape, generator=gen, dtype=torch.float32, device=gen.device)
     return (x * scale).to(dtype)
 
 
 def integers(shape, lo: int, hi: int, dtype: torch.dtype, gen: torch.Generator) -> torch.Tensor:
-    return torch.randint(lo, hi + 1, shape, generator=gen, dtype=torch.int64).to(dtype)
+    return torch.randint(lo, hi + 1, shape, generator=gen, dtype=torch.int64,
+                         device=gen.device).to(dtype)
 
 
 def _mix32(x: torch.Tensor) -> torch.Tensor:
