@@ -72,6 +72,7 @@ class FusedCfg:
     programs: int = 0  # 0: one CTA per SM
     start: int = 0
     stride: int = 1
+    path: str = "auto"  # auto / 1sm / 2sm
 
     def members(self):
         return [self.start + i * self.stride for i in range(self.W)]
@@ -79,8 +80,9 @@ class FusedCfg:
     def describe(self) -> str:
         grp = "" if (self.start, self.stride) == (0, 1) else \
             f" group(start={self.start},stride={self.stride})"
+        kern = "" if self.path == "auto" else f" {self.path}"
         return (f"matmul_all_gather W={self.W} M_local={self.M} N={self.N} K={self.K} "
-                f"{self.dtype} tile 128x256{grp}")
+                f"{self.dtype} tile 128x256{grp}{kern}")
 
 
 ES = {"f16": 2, "bf16": 2, "f32": 4}
@@ -422,12 +424,14 @@ def sweep_points(name: str):
                 pts.append((GatherCfg(W=4, M=M, N=N, dtype="f16", start=1, stride=2,
                                       values="normal"), None))
     elif name == "fused":  # 8 ranks, M_local 1024/4096/16384, f16 and bf16, + subgroup (0,2,4)
-        for M in (1024, 4096, 16384):
-            for dt in ("f16", "bf16"):
-                pts.append((None, replace(FUSED, M=M, dtype=dt)))
-        for M in (4096, 16384):
-            for dt in ("f16", "bf16"):
-                pts.append((None, replace(FUSED, M=M, dtype=dt, W=4, start=0, stride=2)))
+        for path in ("2sm", "1sm"):
+            for M in (1024, 4096, 16384):
+                for dt in ("f16", "bf16"):
+                    pts.append((None, replace(FUSED, M=M, dtype=dt, path=path)))
+            for M in (4096, 16384):
+                for dt in ("f16", "bf16"):
+                    pts.append((None, replace(FUSED, M=M, dtype=dt, W=4, start=0, stride=2,
+                                              path=path)))
     else:
         raise SystemExit(f"unknown sweep {name}")
     return pts
@@ -459,7 +463,7 @@ def run_sweep(args):
                 gg.matmul_all_gather(sh.heap, -1, sh.ptr(f.start, offs["f_a"]), f.K, Bd, f.N,
                                      sh.ptr(f.start, offs["f_out"]), f.N, f.M, f.N, f.K,
                                      gg_inputs.DTYPES[f.dtype], gg.FUSED_TILE, f.programs,
-                                     (f.start, f.stride, f.W), status=status)
+                                     (f.start, f.stride, f.W), status=status, path=f.path)
 
         t_rg, t_rf = roofline_times(peaks, g, f)
         work = t_rg + t_rf
@@ -555,7 +559,7 @@ def main():
             gg.matmul_all_gather(sh.heap, -1, sh.ptr(f.start, offs["f_a"]), f.K, Bd, f.N,
                                  sh.ptr(f.start, offs["f_out"]), f.N, f.M, f.N, f.K, fdt,
                                  gg.FUSED_TILE, f.programs, (f.start, f.stride, f.W),
-                                 status=status, stream=stream)
+                                 status=status, stream=stream, path=f.path)
         if ev is not None:
             ev[2].record(stream)
 
@@ -667,7 +671,8 @@ def main():
                                  "bound": "hbm", "algorithmic_bytes": gather_bytes(g)}
     if f:
         f_tfs = fused_flops(f) / (f_ms * 1e-3) / 1e12
-        kernels["matmul_all_gather"] = {"kernel": "mag_kernel", "ms": f_ms, "TFLOP/s": f_tfs,
+        fk = "mag1_kernel" if (f.path == "1sm" or f.programs < 2) else "mag2_kernel"
+        kernels["matmul_all_gather"] = {"kernel": fk, "ms": f_ms, "TFLOP/s": f_tfs,
                                         "roofline_ms": 1e3 * t_rf, "frac": f_tfs / tc_peak,
                                         "bound": "tensor", "algorithmic_flops": fused_flops(f),
                                         "programs": f.programs}
@@ -679,9 +684,9 @@ def main():
                 "per_unit": "bytes = W*M*N*s reads + W^2*M*N*s writes per launch"}
     else:
         k = kernels["matmul_all_gather"]
-        roof = {"kernel": "mag_kernel", "bound": "tensor", "achieved": k["TFLOP/s"],
+        roof = {"kernel": k["kernel"], "bound": "tensor", "achieved": k["TFLOP/s"],
                 "peak": tc_peak, "unit": "TFLOP/s", "frac": k["frac"],
-                "traffic": traffic_for("mag_kernel", "mag_kernel.cu"),
+                "traffic": traffic_for(k["kernel"], "mag_kernel.cu"),
                 "per_unit": "FLOPs = 2*W*M*N*K per launch"}
     roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peak_src == "measured"
                            else "fallback")

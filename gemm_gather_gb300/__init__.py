@@ -13,7 +13,8 @@ from dataclasses import dataclass
 
 import torch
 
-from ._lib import (GG_AG_AUTO, GG_AG_BULK, GG_AG_VECTOR, GG_BF16, GG_ERR_ALIGNMENT,
+from ._lib import (GG_AG_AUTO, GG_AG_BULK, GG_AG_VECTOR, GG_BF16, GG_MAG_1SM, GG_MAG_2SM,
+                   GG_MAG_AUTO, GG_ERR_ALIGNMENT,
                    GG_ERR_CUDA, GG_ERR_INVALID_ARG, GG_ERR_NOT_IN_HEAP, GG_ERR_TIMEOUT,
                    GG_ERR_UNSUPPORTED, GG_F16, GG_F32, GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N,
                    GG_MAX_WORLD, GG_OK, GGError, Group, Tile, check, lib, LIB_PATH)
@@ -22,11 +23,12 @@ __all__ = [
     "heap_create", "heap_wrap", "heap_bases", "heap_info", "heap_destroy", "all_gather",
     "all_gather_check", "matmul_all_gather", "matmul_all_gather_check", "set_wait_limit_ns",
     "get_wait_limit_ns", "debug_inject_stall", "SymmetricHeap", "Heap", "GGError", "DTYPE_CODES", "PATHS",
-    "FUSED_TILE",
+    "FUSED_TILE", "FUSED_PATHS",
 ]
 
 DTYPE_CODES = {torch.float16: GG_F16, torch.bfloat16: GG_BF16, torch.float32: GG_F32}
 PATHS = {"auto": GG_AG_AUTO, "bulk": GG_AG_BULK, "vector": GG_AG_VECTOR}
+FUSED_PATHS = {"auto": GG_MAG_AUTO, "1sm": GG_MAG_1SM, "2sm": GG_MAG_2SM}
 FUSED_TILE = (GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N)
 
 
@@ -125,10 +127,12 @@ def all_gather_check(heap: Heap, rank: int, input, ld_in: int, output, ld_out: i
 
 def matmul_all_gather(heap: Heap, rank: int, A, lda: int, B, ldb: int, output, ld_out: int,
                       M: int, N: int, K: int, dtype, tile: tuple[int, int], comm_programs: int,
-                      group: tuple[int, int, int], status=None, stream=None) -> None:
-    check(lib.gg_matmul_all_gather(heap.handle, rank, _ptr(A), lda, _ptr(B), ldb, _ptr(output),
-                                   ld_out, M, N, K, _dtype(dtype), Tile(*tile), comm_programs,
-                                   Group(*group), _ptr(status), _stream(stream)))
+                      group: tuple[int, int, int], status=None, stream=None,
+                      path: str = "auto") -> None:
+    check(lib.gg_matmul_all_gather_path(heap.handle, rank, _ptr(A), lda, _ptr(B), ldb,
+                                        _ptr(output), ld_out, M, N, K, _dtype(dtype), Tile(*tile),
+                                        comm_programs, Group(*group), _ptr(status),
+                                        _stream(stream), FUSED_PATHS[path]))
 
 
 def matmul_all_gather_check(heap: Heap, rank: int, A, lda: int, B, ldb: int, output,

@@ -463,12 +463,16 @@ gg_status prepare_fused(const gg_heap *heap, int rank, const void *A, int64_t ld
 
 extern "C" {
 
-gg_status gg_matmul_all_gather(const gg_heap *heap, int rank, const void *A, int64_t lda,
-                               const void *B, int64_t ldb, void *output, int64_t ld_out,
-                               int64_t M, int64_t N, int64_t K, gg_dtype dtype, gg_tile tile,
-                               int comm_programs, gg_group group, int *dev_status,
-                               gg_stream_t stream)
+gg_status gg_matmul_all_gather_path(const gg_heap *heap, int rank, const void *A, int64_t lda,
+                                    const void *B, int64_t ldb, void *output, int64_t ld_out,
+                                    int64_t M, int64_t N, int64_t K, gg_dtype dtype, gg_tile tile,
+                                    int comm_programs, gg_group group, int *dev_status,
+                                    gg_stream_t stream, gg_mag_path path)
 {
+    if (path != GG_MAG_AUTO && path != GG_MAG_1SM && path != GG_MAG_2SM)
+        return fail(GG_ERR_INVALID_ARG, "unknown fused path %d", (int)path);
+    if (path == GG_MAG_2SM && comm_programs < 2)
+        return fail(GG_ERR_INVALID_ARG, "the 2-SM path needs comm_programs >= 2 (one CTA pair)");
     gg::FusedArgs f;
     bool launch = false;
     gg_status st = prepare_fused(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype, tile,
@@ -476,12 +480,22 @@ gg_status gg_matmul_all_gather(const gg_heap *heap, int rank, const void *A, int
     if (st != GG_OK || !launch)
         return st;
     const char *why = nullptr;
-    cudaError_t e = gg::launch_matmul_all_gather(f, comm_programs,
+    cudaError_t e = gg::launch_matmul_all_gather(f, comm_programs, (int)path,
                                                  reinterpret_cast<cudaStream_t>(stream), &why);
     if (e != cudaSuccess)
         return why ? fail(GG_ERR_CUDA, "%s: %s", why, cudaGetErrorName(e))
                    : cuda_fail(e, "launching matmul_all_gather");
     return ok();
+}
+
+gg_status gg_matmul_all_gather(const gg_heap *heap, int rank, const void *A, int64_t lda,
+                               const void *B, int64_t ldb, void *output, int64_t ld_out,
+                               int64_t M, int64_t N, int64_t K, gg_dtype dtype, gg_tile tile,
+                               int comm_programs, gg_group group, int *dev_status,
+                               gg_stream_t stream)
+{
+    return gg_matmul_all_gather_path(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype,
+                                     tile, comm_programs, group, dev_status, stream, GG_MAG_AUTO);
 }
 
 gg_status gg_matmul_all_gather_check(const gg_heap *heap, int rank, const void *A, int64_t lda,

@@ -58,7 +58,8 @@ struct FusedArgs {
     int inject_stall;  // test hook: CTA 0 never arms its first ring stage
 };
 
-cudaError_t launch_matmul_all_gather(const FusedArgs &a, int programs, cudaStream_t s,
+// variant: 0 = automatic (2-SM pairs when programs >= 2), 1 = 1-SM, 2 = 2-SM
+cudaError_t launch_matmul_all_gather(const FusedArgs &a, int programs, int variant, cudaStream_t s,
                                      const char **why);
 
 }  // namespace gg

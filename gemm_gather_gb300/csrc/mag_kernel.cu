@@ -37,19 +37,37 @@ namespace gg {
 namespace {
 
 constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
-constexpr int kStages = 3;
-constexpr int kAStage = BM * BK * 2;            // 16 KB
+constexpr int kAStage = BM * BK * 2;            // 16 KB: 128 rows x 64 K, K-major
 constexpr int kBBox = BK * 64 * 2;              // 8 KB: 64 K-rows x 64 N-columns
-constexpr int kBStage = BK * BN * 2;            // 32 KB
-constexpr int kEpiPitch = BN * 2 + 16;          // staged row pitch (bytes), bank-conflict free
-constexpr int kEpiWarp = 32 * kEpiPitch;        // one epilogue warp's 32 rows
 constexpr int kThreads = 192;                   // 6 warps
 constexpr int kTmemCols = 512;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
+// Geometry of the 1-SM (CG = 1) and 2-SM (CG = 2) variants.  With CG = 2 a
+// CTA pair computes a 256 x 256 tile: each CTA holds its 128 rows of A and
+// one 128-column half of B; the leader CTA's single thread issues
+// tcgen05.mma.cta_group::2 over both CTAs' shared memory and TMEM.
+template <int CG>
+struct Geo {
+    static constexpr int kStages = CG == 1 ? 3 : 5;
+    static constexpr int kBCols = BN / CG;            // B columns one CTA holds
+    static constexpr int kBStage = BK * kBCols * 2;   // 32 KB or 16 KB
+    static constexpr int kTileM = BM * CG;            // rows of one (pair) tile
+    // The epilogue stages each row in column passes of kEpiCols; the staged
+    // row pitch adds 16 bytes so 16-byte stores of 8 consecutive rows hit
+    // distinct banks.
+    static constexpr int kEpiCols = CG == 1 ? 256 : 128;
+    static constexpr int kEpiPitch = kEpiCols * 2 + 16;
+    static constexpr int kEpiWarp = 32 * kEpiPitch;   // one epilogue warp's 32 rows
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kStages * kAStage;
+    static constexpr int kOffEpi = kOffB + kStages * kBStage;
+    static constexpr int kOffShared = kOffEpi + 4 * kEpiWarp;
+};
+
 struct FusedShared {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[5];
+    uint64_t empty[5];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t mma_done;
@@ -58,31 +76,47 @@ struct FusedShared {
     int abort_flag;
 };
 
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kStages * kAStage;
-constexpr int kOffEpi = kOffB + kStages * kBStage;
-constexpr int kOffShared = kOffEpi + 4 * kEpiWarp;
-constexpr int kSmemBytes = kOffShared + (int)sizeof(FusedShared) + 1024;  // + alignment slack
+template <int CG>
+constexpr int smem_bytes()
+{
+    return Geo<CG>::kOffShared + (int)sizeof(FusedShared) + 1024;  // + alignment slack
+}
 
-// ---- tcgen05 / TMA wrappers ---------------------------------------------------
+// ---- tcgen05 / TMA / cluster wrappers --------------------------------------------
+template <int CG>
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
                                             uint32_t bar, uint64_t policy)
 {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
-        "cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
-        : "memory");
+    if constexpr (CG == 1)
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
+            "cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+            : "memory");
+    else  // the barrier may sit in the peer CTA of the pair
+        asm volatile(
+            "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+            "bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+            : "memory");
 }
 
+template <int CG>
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
                                             int c2, uint32_t bar, uint64_t policy)
 {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
-        "cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
-        : "memory");
+    if constexpr (CG == 1)
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::"
+            "cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+            : "memory");
+    else
+        asm volatile(
+            "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+            "bytes.L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+            : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
@@ -92,6 +126,77 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ncluster_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (any CTA of the cluster).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
+                 : "memory");
+}
+
+template <int CG>
+__device__ __forceinline__ void tmem_alloc(uint32_t slot)
+{
+    if constexpr (CG == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    } else {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+}
+
+template <int CG>
+__device__ __forceinline__ void tmem_dealloc(uint32_t tmem)
+{
+    if constexpr (CG == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+}
 
 // Shared-memory matrix descriptor (tcgen05), 128-byte swizzle.
 //   bits  0-13 start address >> 4      bits 16-29 leading byte offset >> 4
@@ -109,34 +214,67 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 }
 
 // Instruction descriptor, kind::f16: D f32, A and B f16 (0) or bf16 (1),
-// A K-major, B N-major, N = 256, M = 128.
-__host__ __device__ constexpr uint32_t instr_desc(int bf16)
+// A K-major, B N-major, N = 256, M = 128 * CG.
+__host__ __device__ constexpr uint32_t instr_desc(int bf16, int cg)
 {
-    return (1u << 4)                      // D format: f32
-           | ((uint32_t)bf16 << 7)        // A format
-           | ((uint32_t)bf16 << 10)       // B format
-           | (0u << 15)                   // A major: K
-           | (1u << 16)                   // B major: MN
-           | ((uint32_t)(BN >> 3) << 17)  // N >> 3
-           | ((uint32_t)(BM >> 4) << 24); // M >> 4
+    return (1u << 4)                           // D format: f32
+           | ((uint32_t)bf16 << 7)             // A format
+           | ((uint32_t)bf16 << 10)            // B format
+           | (0u << 15)                        // A major: K
+           | (1u << 16)                        // B major: MN
+           | ((uint32_t)(BN >> 3) << 17)       // N >> 3
+           | ((uint32_t)((BM * cg) >> 4) << 24); // M >> 4
 }
 
+template <int CG>
 __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
                                         uint32_t idesc, uint32_t accumulate)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if constexpr (CG == 1)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+            "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+            : "memory");
 }
 
-__device__ __forceinline__ void mma_commit(uint32_t bar)
+// Arrive on `bar` once the issuing thread's earlier MMAs are done; with CG = 2
+// the arrival goes to the barrier at that offset in both CTAs of the pair.
+template <int CG>
+__device__ __forceinline__ void mma_commit_all(uint32_t bar)
 {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
+    if constexpr (CG == 1)
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+            "[%0], %1;" ::"r"(bar),
+            "h"((uint16_t)0x3)
+            : "memory");
+}
+
+// Arrive on `bar` in the issuing CTA only.
+template <int CG>
+__device__ __forceinline__ void mma_commit_local(uint32_t bar)
+{
+    if constexpr (CG == 1)
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
+    else
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32])
@@ -218,6 +356,13 @@ __device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+__device__ __forceinline__ void sleep_ns(uint64_t ns)
+{
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < ns)
+        __nanosleep(1000);
+}
+
 struct TileCoord {
     int g;        // group index of the source
     int h;        // heap index of the source
@@ -238,33 +383,38 @@ __device__ __forceinline__ TileCoord tile_coord(const FusedArgs &a, int64_t t, i
     return c;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    mag_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-               const FusedArgs a)
+template <int CG>
+__device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                         const FusedArgs &a)
 {
+    using G = Geo<CG>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-aligned for the 128B swizzle
     uint8_t *smem = smem_raw + (base - raw);
-    FusedShared &sh = *reinterpret_cast<FusedShared *>(smem + kOffShared);
+    FusedShared &sh = *reinterpret_cast<FusedShared *>(smem + G::kOffShared);
     volatile int *abort_flag = &sh.abort_flag;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int tiles_m = (int)((a.M + BM - 1) / BM);
+    const uint32_t rank = CG == 2 ? cluster_ctarank() : 0u;  // position in the CTA pair
+    const bool leader = rank == 0;
+    const int64_t unit = CG == 2 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
+    const int64_t nunits = CG == 2 ? (int64_t)ncluster_x() : (int64_t)gridDim.x;
+    const int tiles_m = (int)((a.M + G::kTileM - 1) / G::kTileM);
     const int tiles_n = (int)((a.N + BN - 1) / BN);
     const int64_t total = (int64_t)a.n_src * tiles_m * tiles_n;
     const int num_kb = (int)((a.K + BK - 1) / BK);
 
     // ---- prologue: barriers, TMEM, destination bases (loaded once) ----------
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < G::kStages; ++s) {
             ptx::mbar_init(ptx::smem_addr(&sh.full[s]), 1);
             ptx::mbar_init(ptx::smem_addr(&sh.empty[s]), 1);
         }
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(ptx::smem_addr(&sh.tmem_full[s]), 1);
-            ptx::mbar_init(ptx::smem_addr(&sh.tmem_empty[s]), 4);
+            ptx::mbar_init(ptx::smem_addr(&sh.tmem_empty[s]), 4 * CG);
         }
         ptx::mbar_init(ptx::smem_addr(&sh.mma_done), 1);
         sh.abort_flag = 0;
@@ -275,16 +425,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&map_b);
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         ptx::smem_addr(&sh.tmem_base)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        tmem_alloc<CG>(ptx::smem_addr(&sh.tmem_base));
         tc_fence_before();
     }
     for (int i = threadIdx.x; i < a.W; i += blockDim.x)
         sh.dst[i] = a.bases[a.rank_start + i * a.rank_stride] + (uint64_t)a.out_off;
     __syncthreads();
+    if constexpr (CG == 2)
+        cluster_sync();  // the peer's barriers exist before anything signals them
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
 
@@ -292,13 +440,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ===================== producer =====================================
         const uint64_t pol_a = ptx::policy_evict_normal();  // A tile: read by tiles_n CTAs
         const uint64_t pol_b = ptx::policy_evict_last();    // B: read by every tile row
+        constexpr uint32_t kTx = CG * (kAStage + G::kBStage);  // bytes of one stage, both CTAs
         int stage = 0;
         uint32_t phase = 0;
         int64_t issued = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int64_t t = unit; t < total && ok; t += nunits) {
             const TileCoord c = tile_coord(a, t, tiles_m, tiles_n);
             const int h_coord = a.a_abs ? 0 : c.h;
+            const int row0 = c.tm * G::kTileM + (int)rank * BM;
+            const int col0 = c.tn * BN + (int)rank * G::kBCols;
             for (int kb = 0; kb < num_kb; ++kb) {
                 const bool got = role_wait(ptx::smem_addr(&sh.empty[stage]), phase ^ 1u,
                                            a.wait_limit_ns, abort_flag);
@@ -306,20 +457,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                const bool stall = a.inject_stall && blockIdx.x == 0 && issued == 0;
+                const bool stall = a.inject_stall && unit == 0 && issued == 0;
                 if (lane == 0 && !stall) {  // test hook: the first stage is never armed
-                    const uint32_t bar = ptx::smem_addr(&sh.full[stage]);
-                    ptx::mbar_arrive_expect_tx(bar, kAStage + kBStage);
-                    const uint32_t sa = base + kOffA + stage * kAStage;
-                    const uint32_t sb = base + kOffB + stage * kBStage;
-                    tma_load_3d(sa, &map_a, kb * BK, c.tm * BM, h_coord, bar, pol_a);
+                    const uint32_t local_full = ptx::smem_addr(&sh.full[stage]);
+                    // every CTA's loads complete on the leader's barrier of this stage
+                    const uint32_t bar = CG == 2 ? map_to_rank(local_full, 0) : local_full;
+                    if (leader)
+                        ptx::mbar_arrive_expect_tx(local_full, kTx);
+                    const uint32_t sa = base + G::kOffA + stage * kAStage;
+                    const uint32_t sb = base + G::kOffB + stage * G::kBStage;
+                    tma_load_3d<CG>(sa, &map_a, kb * BK, row0, h_coord, bar, pol_a);
 #pragma unroll
-                    for (int j = 0; j < BN / 64; ++j)
-                        tma_load_2d(sb + j * kBBox, &map_b, c.tn * BN + j * 64, kb * BK, bar, pol_b);
+                    for (int j = 0; j < G::kBCols / 64; ++j)
+                        tma_load_2d<CG>(sb + j * kBBox, &map_b, col0 + j * 64, kb * BK, bar, pol_b);
                 }
                 __syncwarp();
                 ++issued;
-                if (++stage == kStages) {
+                if (++stage == G::kStages) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -330,23 +484,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             report_status(a.status, kStatusTimeout);
         }
         // drain: every load this warp issued has landed before the CTA may exit
-        const int64_t pending = issued < kStages ? issued : kStages;
-        for (int64_t q = 0; q < pending; ++q) {
-            // the q-th most recent k-block issued
-            const int64_t idx = issued - 1 - q;
-            const int s = (int)(idx % kStages);
-            const uint32_t ph = (uint32_t)((idx / kStages) & 1);
-            ptx::mbar_wait(ptx::smem_addr(&sh.full[s]), ph, kDrainLimitNs);
+        if (leader) {
+            const int64_t pending = issued < G::kStages ? issued : G::kStages;
+            for (int64_t q = 0; q < pending; ++q) {
+                const int64_t idx = issued - 1 - q;  // the q-th most recent k-block
+                const int s = (int)(idx % G::kStages);
+                const uint32_t ph = (uint32_t)((idx / G::kStages) & 1);
+                ptx::mbar_wait(ptx::smem_addr(&sh.full[s]), ph, kDrainLimitNs);
+            }
+        } else if (!ok && issued > 0) {
+            // the peer's loads complete on the leader's barriers, which it cannot
+            // wait on: give copies already in flight time to land
+            sleep_ns(200000);
         }
     } else if (warp == 1) {
-        // ===================== MMA issuer ===================================
-        const uint32_t idesc = instr_desc(a.is_bf16);
+        // ===================== MMA issuer (leader CTA) ======================
+        const uint32_t idesc = instr_desc(a.is_bf16, CG);
         int stage = 0;
         uint32_t phase = 0;
         int64_t lt = 0;  // local tile count
         bool issued_any = false;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < total && ok; t += gridDim.x, ++lt) {
+        for (int64_t t = unit; leader && t < total && ok; t += nunits, ++lt) {
             const int acc = (int)(lt & 1);
             const uint32_t acc_phase = (uint32_t)((lt >> 1) & 1);
             const bool free_acc = role_wait(ptx::smem_addr(&sh.tmem_empty[acc]), acc_phase ^ 1u,
@@ -366,8 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t sa = base + kOffA + stage * kAStage;
-                    const uint32_t sb = base + kOffB + stage * kBStage;
+                    const uint32_t sa = base + G::kOffA + stage * kAStage;
+                    const uint32_t sb = base + G::kOffB + stage * G::kBStage;
 #pragma unroll
                     for (int k = 0; k < BK / UK; ++k) {
                         // A: K-major, +32 bytes per 16-element K step; SBO = 8 rows x 128 B
@@ -375,13 +534,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // B: N-major, +16 K-rows x 128 B per K step; LBO = next 64-column
                         // box, SBO = 8 K-rows x 128 B
                         const uint64_t bd = smem_desc(sb + k * (UK * 128), kBBox, 1024);
-                        mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+                        mma_f16<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                     }
-                    mma_commit(ptx::smem_addr(&sh.empty[stage]));
+                    mma_commit_all<CG>(ptx::smem_addr(&sh.empty[stage]));
                 }
                 __syncwarp();
                 issued_any = true;
-                if (++stage == kStages) {
+                if (++stage == G::kStages) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -389,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok)
                 break;
             if (lane == 0)
-                mma_commit(ptx::smem_addr(&sh.tmem_full[acc]));
+                mma_commit_all<CG>(ptx::smem_addr(&sh.tmem_full[acc]));
             __syncwarp();
         }
         if (!ok) {
@@ -399,20 +558,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // drain: all MMAs of this thread have completed before TMEM is freed
         if (issued_any) {
             if (lane == 0)
-                mma_commit(ptx::smem_addr(&sh.mma_done));
+                mma_commit_local<CG>(ptx::smem_addr(&sh.mma_done));
             __syncwarp();
             ptx::mbar_wait(ptx::smem_addr(&sh.mma_done), 0, kDrainLimitNs);
         }
     } else {
         // ===================== epilogue (warps 2-5) =========================
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const uint32_t stage_row = base + kOffEpi + (uint32_t)(q * kEpiWarp + lane * kEpiPitch);
+        const uint32_t stage_row =
+            base + G::kOffEpi + (uint32_t)(q * G::kEpiWarp + lane * G::kEpiPitch);
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         const int64_t ld_out_b = a.ld_out * 2;
         const uint64_t pol_c = ptx::policy_evict_first();  // output: written once, never read
         int64_t lt = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < total; t += gridDim.x, ++lt) {
+        for (int64_t t = unit; t < total; t += nunits, ++lt) {
             const TileCoord c = tile_coord(a, t, tiles_m, tiles_n);
             const int acc = (int)(lt & 1);
             const uint32_t acc_phase = (uint32_t)((lt >> 1) & 1);
@@ -423,53 +583,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            // this warp's staging rows are free once its previous stores have read them
-            ptx::bulk_wait_read<0>();
-            __syncwarp();
             const uint32_t t_addr = tmem + lane_addr + (uint32_t)(acc * BN);
+            const int64_t row = (int64_t)c.tm * G::kTileM + (int64_t)rank * BM + q * 32 + lane;
+            const int64_t row_off = ((int64_t)c.g * a.M + row) * ld_out_b;
 #pragma unroll 1
-            for (int cb = 0; cb < BN; cb += 64) {
-                uint32_t v0[32], v1[32];
-                tmem_ld_32x32b_x32(t_addr + (uint32_t)cb, v0);
-                tmem_ld_32x32b_x32(t_addr + (uint32_t)(cb + 32), v1);
-                tmem_wait_ld(v0);
-                reg_order(v1);
+            for (int pass = 0; pass < BN; pass += G::kEpiCols) {
+                // this thread's staging row is free once its previous stores have read it
+                ptx::bulk_wait_read<0>();
+#pragma unroll 1
+                for (int cb = 0; cb < G::kEpiCols; cb += 64) {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld_32x32b_x32(t_addr + (uint32_t)(pass + cb), v0);
+                    tmem_ld_32x32b_x32(t_addr + (uint32_t)(pass + cb + 32), v1);
+                    tmem_wait_ld(v0);
+                    reg_order(v1);
 #pragma unroll
-                for (int j = 0; j < 32; j += 8)
-                    st_shared_v4(stage_row + (uint32_t)(cb * 2 + j * 2), pack2(v0[j], v0[j + 1], a.is_bf16),
-                                 pack2(v0[j + 2], v0[j + 3], a.is_bf16),
-                                 pack2(v0[j + 4], v0[j + 5], a.is_bf16),
-                                 pack2(v0[j + 6], v0[j + 7], a.is_bf16));
+                    for (int j = 0; j < 32; j += 8)
+                        st_shared_v4(stage_row + (uint32_t)(cb * 2 + j * 2),
+                                     pack2(v0[j], v0[j + 1], a.is_bf16),
+                                     pack2(v0[j + 2], v0[j + 3], a.is_bf16),
+                                     pack2(v0[j + 4], v0[j + 5], a.is_bf16),
+                                     pack2(v0[j + 6], v0[j + 7], a.is_bf16));
 #pragma unroll
-                for (int j = 0; j < 32; j += 8)
-                    st_shared_v4(stage_row + (uint32_t)((cb + 32) * 2 + j * 2),
-                                 pack2(v1[j], v1[j + 1], a.is_bf16),
-                                 pack2(v1[j + 2], v1[j + 3], a.is_bf16),
-                                 pack2(v1[j + 4], v1[j + 5], a.is_bf16),
-                                 pack2(v1[j + 6], v1[j + 7], a.is_bf16));
-            }
-            // accumulator fully read: hand it back to the MMA warp
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                ptx::mbar_arrive(ptx::smem_addr(&sh.tmem_empty[acc]));
-            // staged rows -> every destination, local first, peers rotated
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            const int64_t row = (int64_t)c.tm * BM + q * 32 + lane;
-            const int64_t col0 = (int64_t)c.tn * BN;
-            if (row < a.M) {
-                const uint32_t rb = (uint32_t)(gg_min64(BN, a.N - col0) * 2);
-                const int64_t off = ((int64_t)c.g * a.M + row) * ld_out_b + col0 * 2;
-                for (int j = 0; j < a.W; ++j) {
-                    int i = c.g + j;
-                    if (i >= a.W)
-                        i -= a.W;
-                    ptx::bulk_s2g_hint(reinterpret_cast<uint8_t *>(sh.dst[i]) + off, stage_row, rb,
-                                       pol_c);
+                    for (int j = 0; j < 32; j += 8)
+                        st_shared_v4(stage_row + (uint32_t)((cb + 32) * 2 + j * 2),
+                                     pack2(v1[j], v1[j + 1], a.is_bf16),
+                                     pack2(v1[j + 2], v1[j + 3], a.is_bf16),
+                                     pack2(v1[j + 4], v1[j + 5], a.is_bf16),
+                                     pack2(v1[j + 6], v1[j + 7], a.is_bf16));
                 }
+                if (pass + G::kEpiCols >= BN) {
+                    // accumulator fully read: hand it back to the (leader's) MMA warp
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const uint32_t e = ptx::smem_addr(&sh.tmem_empty[acc]);
+                        if constexpr (CG == 2)
+                            mbar_arrive_cluster(map_to_rank(e, 0));
+                        else
+                            ptx::mbar_arrive(e);
+                    }
+                }
+                // staged row segment -> every destination, local first, peers rotated
+                ptx::fence_proxy_async_smem();
+                const int64_t col0 = (int64_t)c.tn * BN + pass;
+                if (row < a.M && col0 < a.N) {
+                    const uint32_t rb = (uint32_t)(gg_min64(G::kEpiCols, a.N - col0) * 2);
+                    const int64_t off = row_off + col0 * 2;
+                    for (int j = 0; j < a.W; ++j) {
+                        int i = c.g + j;
+                        if (i >= a.W)
+                            i -= a.W;
+                        ptx::bulk_s2g_hint(reinterpret_cast<uint8_t *>(sh.dst[i]) + off, stage_row,
+                                           rb, pol_c);
+                    }
+                }
+                ptx::bulk_commit();
             }
-            ptx::bulk_commit();
         }
         if (!ok) {
             *abort_flag = 1;
@@ -481,12 +651,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- teardown ---------------------------------------------------------------
     tc_fence_before();
     __syncthreads();
+    if constexpr (CG == 2)
+        cluster_sync();  // the leader's MMAs into the peer's TMEM and smem are done
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                     "r"(kTmemCols)
-                     : "memory");
+        tmem_dealloc<CG>(tmem);
     }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mag1_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                const FusedArgs a)
+{
+    mag_body<1>(map_a, map_b, a);
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    mag2_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                const FusedArgs a)
+{
+    mag_body<2>(map_a, map_b, a);
 }
 
 // ---- host: tensor maps and launch ------------------------------------------------
@@ -512,7 +696,7 @@ EncodeTiledFn encode_fn()
 
 }  // namespace
 
-cudaError_t launch_matmul_all_gather(const FusedArgs &a, int programs, cudaStream_t s,
+cudaError_t launch_matmul_all_gather(const FusedArgs &a, int programs, int variant, cudaStream_t s,
                                      const char **why)
 {
     EncodeTiledFn enc = encode_fn();
@@ -555,15 +739,51 @@ cudaError_t launch_matmul_all_gather(const FusedArgs &a, int programs, cudaStrea
             return cudaErrorInvalidValue;
         }
     }
-    cudaError_t e =
-        cudaFuncSetAttribute(mag_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) {
-        *why = "setting the shared-memory size of the fused kernel";
-        return e;
+    const int64_t tiles_n = (a.N + BN - 1) / BN;
+    const bool two_sm = variant != 1 && programs >= 2;
+    cudaError_t e;
+    if (two_sm) {
+        const int64_t pairs = (int64_t)a.n_src * ((a.M + 2 * BM - 1) / (2 * BM)) * tiles_n;
+        e = cudaFuncSetAttribute(mag2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes<2>());
+        if (e != cudaSuccess) {
+            *why = "setting the shared-memory size of the fused kernel";
+            return e;
+        }
+        // persistent pairs: never more clusters than can be resident at once
+        int resident = 0;
+        {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(2 * (unsigned)gg_min64(programs / 2, pairs), 1, 1);
+            cfg.blockDim = dim3(kThreads, 1, 1);
+            cfg.dynamicSmemBytes = smem_bytes<2>();
+            cfg.stream = s;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&resident, mag2_kernel, &cfg) != cudaSuccess)
+                resident = 0;
+            (void)cudaGetLastError();
+        }
+        int64_t clusters = gg_min64(programs / 2, pairs);
+        if (resident > 0)
+            clusters = gg_min64(clusters, resident);
+        mag2_kernel<<<(int)(2 * clusters), kThreads, smem_bytes<2>(), s>>>(map_a, map_b, a);
+    } else {
+        const int64_t tiles = (int64_t)a.n_src * ((a.M + BM - 1) / BM) * tiles_n;
+        e = cudaFuncSetAttribute(mag1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes<1>());
+        if (e != cudaSuccess) {
+            *why = "setting the shared-memory size of the fused kernel";
+            return e;
+        }
+        mag1_kernel<<<(int)gg_min64(programs, tiles), kThreads, smem_bytes<1>(), s>>>(map_a, map_b,
+                                                                                    a);
     }
-    const int64_t tiles = (int64_t)a.n_src * ((a.M + BM - 1) / BM) * ((a.N + BN - 1) / BN);
-    const int grid = (int)(programs < tiles ? programs : tiles);
-    mag_kernel<<<grid, kThreads, kSmemBytes, s>>>(map_a, map_b, a);
     return cudaGetLastError();
 }
 

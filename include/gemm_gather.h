@@ -179,6 +179,9 @@ gg_status gg_all_gather_check(const gg_heap *heap, int rank, const void *input, 
  * Alignment (GG_ERR_ALIGNMENT otherwise): A, B, output 16-byte aligned;
  *   lda, ldb, ld_out multiples of 8; N a multiple of 8.
  * comm_programs: number of persistent CTAs (one per SM at most is useful).
+ *   By default they run as CTA pairs (comm_programs/2 clusters of two CTAs,
+ *   a 256 x 256 output tile per pair); a single program runs alone on
+ *   128 x 256 tiles.
  * M, N or K == 0: nothing is launched, GG_OK (with K == 0 nothing is
  *   written either).
  * ------------------------------------------------------------------------- */
@@ -187,6 +190,19 @@ gg_status gg_matmul_all_gather(const gg_heap *heap, int rank, const void *A, int
                                int64_t M, int64_t N, int64_t K, gg_dtype dtype,
                                gg_tile tile, int comm_programs, gg_group group,
                                int *dev_status, gg_stream_t stream);
+
+/* Kernel variants of gg_matmul_all_gather (same arguments and result):
+ *   GG_MAG_AUTO  2-SM pairs when comm_programs >= 2, else 1-SM
+ *   GG_MAG_1SM   one CTA per 128 x 256 tile (tcgen05.mma.cta_group::1)
+ *   GG_MAG_2SM   a CTA pair per 256 x 256 tile (tcgen05.mma.cta_group::2);
+ *                needs comm_programs >= 2 (else GG_ERR_INVALID_ARG) */
+typedef enum { GG_MAG_AUTO = 0, GG_MAG_1SM = 1, GG_MAG_2SM = 2 } gg_mag_path;
+
+gg_status gg_matmul_all_gather_path(const gg_heap *heap, int rank, const void *A, int64_t lda,
+                                    const void *B, int64_t ldb, void *output, int64_t ld_out,
+                                    int64_t M, int64_t N, int64_t K, gg_dtype dtype, gg_tile tile,
+                                    int comm_programs, gg_group group, int *dev_status,
+                                    gg_stream_t stream, gg_mag_path path);
 
 /* Validate a gg_matmul_all_gather call exactly as the launching call does
  * and launch nothing. */

@@ -60,7 +60,8 @@ def test_gather_wait_limit_reports_timeout(oracle, short_waits):
     assert np.array_equal(got, host), first_diff(got, host, lay)
 
 
-def test_fused_wait_limit_reports_timeout(oracle, short_waits):
+@pytest.mark.parametrize("path", ["1sm", "2sm"])
+def test_fused_wait_limit_reports_timeout(oracle, short_waits, path):
     import gemm_gather_gb300 as gg
     W, M, N, K = 2, 512, 1024, 2048
     lay = hi.make_layout(W, W, M, N, 2, ld_in=K)
@@ -74,14 +75,16 @@ def test_fused_wait_limit_reports_timeout(oracle, short_waits):
     Bd = B.to("cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     gg.matmul_all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), K, Bd, N, sh.ptr(0, lay.out_off), N,
-                         M, N, K, torch.float16, gg.FUSED_TILE, 8, (0, 1, W), status=status)
+                         M, N, K, torch.float16, gg.FUSED_TILE, 8, (0, 1, W), status=status,
+                         path=path)
     torch.cuda.synchronize()
     assert int(status.item()) == TIMEOUT
     gg.debug_inject_stall(False)
     gg.set_wait_limit_ns(0)
     status.zero_()
     gg.matmul_all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), K, Bd, N, sh.ptr(0, lay.out_off), N,
-                         M, N, K, torch.float16, gg.FUSED_TILE, 8, (0, 1, W), status=status)
+                         M, N, K, torch.float16, gg.FUSED_TILE, 8, (0, 1, W), status=status,
+                         path=path)
     got = download(sh)
     assert int(status.item()) == 0
     oracle.matmul_all_gather(host, lay.part_bytes, lay.in_off, K,

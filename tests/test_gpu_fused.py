@@ -45,7 +45,7 @@ def check_tolerance(gpu_vals: np.ndarray, ref: np.ndarray, dtype) -> None:
 
 
 def run_fused(oracle, H, group, M, N, K, dtype, programs, values="int", lda_pad=0,
-              ld_out_pad=0, mode="group", seed=0):
+              ld_out_pad=0, mode="group", seed=0, path="auto"):
     import gemm_gather_gb300 as gg
     start, stride, W = group
     members = [start + i * stride for i in range(W)]
@@ -72,12 +72,12 @@ def run_fused(oracle, H, group, M, N, K, dtype, programs, values="int", lda_pad=
     if mode == "group":
         gg.matmul_all_gather(sh.heap, -1, sh.ptr(members[0], lay.in_off), lda, Bd, N,
                              sh.ptr(members[0], lay.out_off), lay.ld_out, M, N, K, dtype,
-                             gg.FUSED_TILE, programs, group, status=status)
+                             gg.FUSED_TILE, programs, group, status=status, path=path)
     else:
         for h in members:
             gg.matmul_all_gather(sh.heap, h, sh.ptr(h, lay.in_off), lda, Bd, N,
                                  sh.ptr(h, lay.out_off), lay.ld_out, M, N, K, dtype,
-                                 gg.FUSED_TILE, programs, group, status=status)
+                                 gg.FUSED_TILE, programs, group, status=status, path=path)
     got = download(sh)
     assert int(status.item()) == 0, int(status.item())
     prods = oracle.matmul_all_gather(host, lay.part_bytes, lay.in_off, lda, _bits(B),
@@ -111,24 +111,32 @@ INT_CASES = [
 ]
 
 
+PATHS = ["1sm", "2sm"]
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
 @pytest.mark.parametrize("case", INT_CASES, ids=lambda c: f"H{c[0]}g{c[1]}_{c[2]}x{c[3]}x{c[4]}p{c[5]}")
-def test_integer_operands_bit_exact(oracle, case, dtype):
+def test_integer_operands_bit_exact(oracle, case, dtype, path):
     H, group, M, N, K, programs, lp, op = case
-    run_fused(oracle, H, group, M, N, K, dtype, programs, "int", lp, op)
+    if path == "2sm" and programs < 2:
+        programs = 2
+    run_fused(oracle, H, group, M, N, K, dtype, programs, "int", lp, op, path=path)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
 @pytest.mark.parametrize("shape", [(256, 512, 1024), (130, 264, 520), (512, 1024, 2048)])
-def test_random_operands_within_tolerance(oracle, shape, dtype):
+def test_random_operands_within_tolerance(oracle, shape, dtype, path):
     M, N, K = shape
-    run_fused(oracle, 3, (0, 1, 3), M, N, K, dtype, 7, "normal")
+    run_fused(oracle, 3, (0, 1, 3), M, N, K, dtype, 7, "normal", path=path)
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
-def test_single_rank_launches(oracle, dtype):
-    run_fused(oracle, 4, (0, 1, 4), 160, 512, 192, dtype, 5, "int", mode="ranks")
-    run_fused(oracle, 6, (1, 2, 3), 96, 256, 320, dtype, 3, "normal", mode="ranks")
+def test_single_rank_launches(oracle, dtype, path):
+    run_fused(oracle, 4, (0, 1, 4), 160, 512, 192, dtype, 5, "int", mode="ranks", path=path)
+    run_fused(oracle, 6, (1, 2, 3), 96, 256, 320, dtype, 3, "normal", mode="ranks", path=path)
 
 
 def test_zero_k_writes_nothing():
