@@ -58,8 +58,9 @@ class GatherCfg:
     def describe(self) -> str:
         grp = "" if (self.start, self.stride) == (0, 1) else \
             f" group(start={self.start},stride={self.stride})"
+        kern = "" if self.path == "auto" else f" {self.path}"
         return (f"all_gather W={self.W} {self.M}x{self.N} {self.dtype} tile {self.bm}x{self.bn} "
-                f"{self.programs} programs{grp}")
+                f"{self.programs} programs{grp}{kern}")
 
 
 @dataclass
@@ -407,9 +408,10 @@ def setup_device(dev, g: GatherCfg | None, f: FusedCfg | None, device_inputs: bo
 def sweep_points(name: str):
     """(GatherCfg | None, FusedCfg | None) points of the configuration sweeps."""
     pts = []
-    if name == "budget":  # 8 ranks, 4096x4096 f16, tile 8x256, budget swept
-        for p in (8, 16, 32, 64, 148):
-            pts.append((replace(GATHER, programs=p), None))
+    if name == "budget":  # 8 ranks, 4096x4096 f16, tile 8x256, budget swept, every data path
+        for path in ("tma", "bulk", "vector"):
+            for p in (8, 16, 32, 64, 148):
+                pts.append((replace(GATHER, programs=p, path=path), None))
     elif name == "gather":  # 4 and 8 ranks, M x N x dtype x tile x budget, normal values
         for W in (4, 8):
             for M in (1024, 4096, 16384):
@@ -665,7 +667,7 @@ def main():
     kernels = {}
     if g:
         g_gbs = gather_bytes(g) / (g_ms * 1e-3) / 1e9
-        kname = "ag_vec_kernel" if g.path == "vector" else "ag_bulk_kernel"
+        kname = {"vector": "ag_vec_kernel", "bulk": "ag_bulk_kernel"}.get(g.path, "ag_tma_kernel")
         kernels["all_gather"] = {"kernel": kname, "ms": g_ms, "GB/s": g_gbs,
                                  "roofline_ms": 1e3 * t_rg, "frac": g_gbs / hbm_peak,
                                  "bound": "hbm", "algorithmic_bytes": gather_bytes(g)}

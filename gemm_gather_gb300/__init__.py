@@ -13,7 +13,7 @@ from dataclasses import dataclass
 
 import torch
 
-from ._lib import (GG_AG_AUTO, GG_AG_BULK, GG_AG_VECTOR, GG_BF16, GG_MAG_1SM, GG_MAG_2SM,
+from ._lib import (GG_AG_AUTO, GG_AG_BULK, GG_AG_TMA, GG_AG_VECTOR, GG_BF16, GG_MAG_1SM, GG_MAG_2SM,
                    GG_MAG_AUTO, GG_ERR_ALIGNMENT,
                    GG_ERR_CUDA, GG_ERR_INVALID_ARG, GG_ERR_NOT_IN_HEAP, GG_ERR_TIMEOUT,
                    GG_ERR_UNSUPPORTED, GG_F16, GG_F32, GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N,
@@ -27,7 +27,7 @@ __all__ = [
 ]
 
 DTYPE_CODES = {torch.float16: GG_F16, torch.bfloat16: GG_BF16, torch.float32: GG_F32}
-PATHS = {"auto": GG_AG_AUTO, "bulk": GG_AG_BULK, "vector": GG_AG_VECTOR}
+PATHS = {"auto": GG_AG_AUTO, "bulk": GG_AG_BULK, "vector": GG_AG_VECTOR, "tma": GG_AG_TMA}
 FUSED_PATHS = {"auto": GG_MAG_AUTO, "1sm": GG_MAG_1SM, "2sm": GG_MAG_2SM}
 FUSED_TILE = (GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N)
 
@@ -122,7 +122,8 @@ def all_gather_check(heap: Heap, rank: int, input, ld_in: int, output, ld_out: i
     check(lib.gg_all_gather_check(heap.handle, rank, _ptr(input), ld_in, _ptr(output), ld_out, M,
                                   N, _dtype(dtype), Tile(*tile), comm_programs, Group(*group),
                                   PATHS[path], ctypes.byref(chosen)))
-    return {GG_AG_AUTO: "none", GG_AG_BULK: "bulk", GG_AG_VECTOR: "vector"}[chosen.value]
+    return {GG_AG_AUTO: "none", GG_AG_BULK: "bulk", GG_AG_VECTOR: "vector",
+            GG_AG_TMA: "tma"}[chosen.value]
 
 
 def matmul_all_gather(heap: Heap, rank: int, A, lda: int, B, ldb: int, output, ld_out: int,

@@ -20,7 +20,7 @@ GG_ERR_CUDA = -5
 GG_ERR_TIMEOUT = -6
 
 GG_F16, GG_BF16, GG_F32 = 0, 1, 2
-GG_AG_AUTO, GG_AG_BULK, GG_AG_VECTOR = 0, 1, 2
+GG_AG_AUTO, GG_AG_BULK, GG_AG_VECTOR, GG_AG_TMA = 0, 1, 2, 3
 GG_MAG_AUTO, GG_MAG_1SM, GG_MAG_2SM = 0, 1, 2
 GG_MAX_WORLD = 64
 GG_MAX_HEAPS = 1024

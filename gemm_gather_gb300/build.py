@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgemm_gather.so")
-SOURCES = ["gg_api.cu", "ag_kernels.cu", "mag_kernel.cu"]
+SOURCES = ["gg_api.cu", "ag_kernels.cu", "mag_kernel.cu", "tensor_maps.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

@@ -12,13 +12,21 @@
 //    rotated order (i+1, i+2, ... mod W), with no fence or reload between
 //    destinations.
 //
-// Two data paths with identical results:
+// Three data paths with identical results:
+//  * tma:    one TMA tensor load per tile into shared memory (mbarrier
+//            completion) and one TMA tensor store per tile and destination,
+//            through per-member tensor maps built on the host from the
+//            heap-bases table once per launch (the translation hoisted out of
+//            every loop; each map views a member's output as {N, M, W} so a
+//            tile is clipped at the end of its row block).  Same pipeline as
+//            the bulk path.
 //  * bulk:   tiles are staged in shared memory by the TMA engine
 //            (cp.async.bulk, completion on an mbarrier) and stored with
 //            cp.async.bulk shared->global, one copy per tile row and
-//            destination.  Four warps per program run independent pipelines
-//            over a ring of stages; a stage is refilled once the stores that
-//            read it have finished reading shared memory.
+//            destination.  Each warp of a program runs an independent
+//            pipeline over a ring of stages (the warps per program follow the
+//            budget, see kAgTargetPipes); a stage is refilled once the stores
+//            that read it have finished reading shared memory.
 //  * vector: 16/8/4/2-byte loads into registers, then one store per
 //            destination; several tiles' loads are in flight per thread.
 #include <cuda_runtime.h>
@@ -29,7 +37,11 @@
 namespace gg {
 namespace {
 
-constexpr int kAgWarps = 4;           // most independent pipelines (warps) per program
+constexpr int kAgWarps = 8;           // most independent pipelines (warps) per program
+// Pipelines the whole launch aims for: each program runs about
+// kAgTargetPipes / programs of them (1..kAgWarps), so a small budget still
+// keeps enough copies in flight and a large one does not oversubscribe.
+constexpr int kAgTargetPipes = 512;
 constexpr int kAgMaxStages = 16;      // ring stages per pipeline
 constexpr int kAgSmemBudget = 192 * 1024;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;  // waits for copies already in flight
@@ -62,6 +74,31 @@ __device__ __forceinline__ Item decode_item(const GatherArgs &a, int64_t t)
     const int64_t c0 = it.tn * a.bn_b;
     it.rb = (uint32_t)gg_min64(a.bn_b, a.row_b - c0);
     return it;
+}
+
+__device__ __forceinline__ void tma_prefetch(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                             int c2, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+        "[%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_box(const CUtensorMap *map, uint32_t src, int c0, int c1,
+                                              int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
 }
 
 // Heap bases -> per-member input and output bases, once per program.
@@ -175,6 +212,98 @@ __global__ void __launch_bounds__(kAgWarps * 32)
     ptx::bulk_wait_all();
 }
 
+// Tensor-map path: same ring pipeline as ag_bulk_kernel; a tile is one box.
+template <int D>
+__global__ void __launch_bounds__(kAgWarps * 32)
+    ag_tma_kernel(const __grid_constant__ CUtensorMap in_map, const __grid_constant__ OutMaps out,
+                  const GatherArgs a, int stages, int stage_bytes)
+{
+    const int npipe = blockDim.x >> 5;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    AgShared &sh = *reinterpret_cast<AgShared *>(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int w = 0; w < npipe; ++w)
+            for (int s = 0; s < stages; ++s)
+                ptx::mbar_init(ptx::smem_addr(&sh.full[w][s]), 1);
+        ptx::fence_barrier_init();
+        tma_prefetch(&in_map);
+    }
+    if (threadIdx.x < (unsigned)a.W)
+        tma_prefetch(&out.map[threadIdx.x]);
+    __syncthreads();
+
+    const int64_t step = (int64_t)gridDim.x * npipe;
+    const int64_t first = blockIdx.x + (int64_t)warp * gridDim.x;
+    const int64_t n_local = first < a.total_items ? (a.total_items - 1 - first) / step + 1 : 0;
+    const int lookahead = stages - D;
+    const uint32_t ring = ptx::smem_addr(smem + kAgHeader) + (uint32_t)(warp * stages * stage_bytes);
+    const uint32_t full0 = ptx::smem_addr(&sh.full[warp][0]);
+    const uint32_t box_bytes = (uint32_t)(a.bm * a.bn_b);  // a full box, clipped parts zero-filled
+    const int bn = (int)(a.bn_b / a.es);
+
+    auto issue_load = [&](int64_t k) {
+        const Item it = decode_item(a, first + k * step);
+        const int st = (int)(k % stages);
+        const uint32_t bar = full0 + 8u * st;
+        if (a.inject_stall && k == 0 && blockIdx.x == 0 && warp == 0)
+            return;  // test hook: this stage's barrier phase never completes
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bar, box_bytes);
+            const int h = a.in_abs ? 0 : a.rank_start + it.g * a.rank_stride;
+            tma_load_box(ring + (uint32_t)st * stage_bytes, &in_map, (int)it.tn * bn,
+                         (int)(it.tm * a.bm), h, bar);
+        }
+        __syncwarp();
+    };
+
+    const int64_t preload = gg_min64(lookahead, n_local);
+    for (int64_t k = 0; k < preload; ++k)
+        issue_load(k);
+
+    int64_t k = 0;
+    bool ok = true;
+    for (; k < n_local; ++k) {
+        const int st = (int)(k % stages);
+        const uint32_t parity = (uint32_t)((k / stages) & 1);
+        const bool mine = ptx::mbar_wait(full0 + 8u * st, parity, a.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, mine)) {
+            ok = false;
+            break;
+        }
+        const Item it = decode_item(a, first + k * step);
+        const uint32_t buf = ring + (uint32_t)st * stage_bytes;
+        // lane j stores the tile to destination j: the local copy first, peers rotated
+        for (int j = lane; j < a.W; j += 32) {
+            int i = it.g + j;
+            if (i >= a.W)
+                i -= a.W;
+            tma_store_box(&out.map[i], buf, (int)it.tn * bn, (int)(it.tm * a.bm), it.g);
+        }
+        ptx::bulk_commit();
+        const int64_t kk = k + lookahead;
+        if (kk < n_local) {
+            if (kk >= stages) {
+                ptx::bulk_wait_read<D>();
+                __syncwarp();
+            }
+            issue_load(kk);
+        }
+    }
+
+    if (!ok) {
+        report_status(a.status, kStatusTimeout);
+        const int64_t end = gg_min64(k + lookahead, n_local);
+        for (int64_t q = k; q < end; ++q) {
+            const int st = (int)(q % stages);
+            ptx::mbar_wait(full0 + 8u * st, (uint32_t)((q / stages) & 1), kDrainLimitNs);
+        }
+    }
+    ptx::bulk_wait_all();
+}
+
 template <int VB>
 struct VecType;
 template <>
@@ -243,22 +372,24 @@ __global__ void __launch_bounds__(kVecThreads) ag_vec_kernel(const GatherArgs a)
 
 }  // namespace
 
-// Ring geometry of the bulk path for a tile of `stage_raw` bytes: pipelines
-// per program, stages per pipeline and read depth D.  False if it cannot fit.
-bool bulk_geometry(int64_t stage_raw, int *npipe, int *stages, int *depth, int *stage_bytes)
+// Ring geometry for a tile of `stage_raw` bytes and `programs` programs:
+// pipelines (warps) per program, stages per pipeline and read depth D.
+// False if not even one pipeline of three stages fits.
+bool ring_geometry(int64_t stage_raw, int programs, int *npipe, int *stages, int *depth,
+                   int *stage_bytes)
 {
     const int64_t sb = (stage_raw + 1023) / 1024 * 1024;
-    for (int np = kAgWarps; np >= 1; np >>= 1) {
+    int want = (kAgTargetPipes + programs - 1) / programs;
+    want = want < 1 ? 1 : (want > kAgWarps ? kAgWarps : want);
+    for (int np = want; np >= 1; --np) {
         const int64_t st = gg_min64(kAgMaxStages, (kAgSmemBudget - kAgHeader) / (np * sb));
-        if (st >= 6) {
-            *npipe = np; *stages = (int)st; *depth = 4; *stage_bytes = (int)sb;
+        if (st >= 3) {
+            *npipe = np;
+            *stages = (int)st;
+            *depth = st >= 6 ? 4 : (st >= 4 ? 2 : 1);
+            *stage_bytes = (int)sb;
             return true;
         }
-    }
-    const int64_t st = gg_min64(kAgMaxStages, (kAgSmemBudget - kAgHeader) / sb);
-    if (st >= 3) {
-        *npipe = 1; *stages = (int)st; *depth = st >= 4 ? 2 : 1; *stage_bytes = (int)sb;
-        return true;
     }
     return false;
 }
@@ -276,10 +407,37 @@ static cudaError_t launch_bulk_depth(const GatherArgs &a, int programs, int npip
     return cudaGetLastError();
 }
 
+template <int D>
+static cudaError_t launch_tma_depth(const CUtensorMap &in_map, const OutMaps &out,
+                                    const GatherArgs &a, int programs, int npipe, int stages,
+                                    int stage_bytes, cudaStream_t s)
+{
+    const int smem = kAgHeader + npipe * stages * stage_bytes;
+    cudaError_t e =
+        cudaFuncSetAttribute(ag_tma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess)
+        return e;
+    ag_tma_kernel<D><<<programs, npipe * 32, smem, s>>>(in_map, out, a, stages, stage_bytes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather_tma(const CUtensorMap &in_map, const OutMaps &out, const GatherArgs &a,
+                              int programs, cudaStream_t s)
+{
+    int npipe, stages, depth, stage_bytes;
+    if (!ring_geometry((int64_t)a.bm * a.bn_b, programs, &npipe, &stages, &depth, &stage_bytes))
+        return cudaErrorInvalidValue;
+    switch (depth) {
+    case 4: return launch_tma_depth<4>(in_map, out, a, programs, npipe, stages, stage_bytes, s);
+    case 2: return launch_tma_depth<2>(in_map, out, a, programs, npipe, stages, stage_bytes, s);
+    default: return launch_tma_depth<1>(in_map, out, a, programs, npipe, stages, stage_bytes, s);
+    }
+}
+
 cudaError_t launch_gather_bulk(const GatherArgs &a, int programs, cudaStream_t s)
 {
     int npipe, stages, depth, stage_bytes;
-    if (!bulk_geometry((int64_t)a.bm * a.bn_b, &npipe, &stages, &depth, &stage_bytes))
+    if (!ring_geometry((int64_t)a.bm * a.bn_b, programs, &npipe, &stages, &depth, &stage_bytes))
         return cudaErrorInvalidValue;  // tile too large (the host validates first)
     switch (depth) {
     case 4: return launch_bulk_depth<4>(a, programs, npipe, stages, stage_bytes, s);

@@ -204,10 +204,14 @@ namespace {
 
 // Validation and argument set-up of a gather; *launch is false when there is
 // nothing to do (M == 0 or N == 0).
+// Data path a gather launch takes.
+enum GatherKind { kVector = 0, kBulk = 1, kTma = 2 };
+
 gg_status prepare_gather(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
                          void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
                          gg_tile tile, int comm_programs, gg_group group, int *dev_status,
-                         gg_ag_path path, gg::GatherArgs *out_args, int *vec_bytes, bool *launch)
+                         gg_ag_path path, gg::GatherArgs *out_args, int *kind, int *vec_bytes,
+                         CUtensorMap *in_map, gg::OutMaps *maps, bool *launch)
 {
     *launch = false;
     int gi = -1;
@@ -217,7 +221,7 @@ gg_status prepare_gather(const gg_heap *heap, int rank, const void *input, int64
     const int es = elem_size(dtype);
     if (es == 0)
         return fail(GG_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
-    if (path != GG_AG_AUTO && path != GG_AG_BULK && path != GG_AG_VECTOR)
+    if (path != GG_AG_AUTO && path != GG_AG_BULK && path != GG_AG_VECTOR && path != GG_AG_TMA)
         return fail(GG_ERR_INVALID_ARG, "unknown path %d", (int)path);
     if (M < 0 || N < 0)
         return fail(GG_ERR_INVALID_ARG, "M and N must be >= 0");
@@ -246,7 +250,7 @@ gg_status prepare_gather(const gg_heap *heap, int rank, const void *input, int64
         !checked_mul(tmp + N, es, &out_ext) || !checked_mul(M - 1, ld_in, &tmp) ||
         !checked_mul(tmp + N, es, &in_ext))
         return fail(GG_ERR_INVALID_ARG, "sizes overflow");
-    int64_t out_off;
+    int64_t out_off = 0;
     st = symmetric_offset(heap, output, out_ext, "output", &out_off);
     if (st != GG_OK)
         return st;
@@ -292,6 +296,7 @@ gg_status prepare_gather(const gg_heap *heap, int rank, const void *input, int64
     a.tiles_n = ceil_div(N, tile.block_n);
     a.tiles_per_src = ceil_div(M, tile.block_m) * a.tiles_n;
     a.total_items = a.tiles_per_src * a.n_src;
+    a.es = es;
     a.status = dev_status;
     a.wait_limit_ns = g_wait_limit_ns.load();
     a.inject_stall = g_inject_stall.load();
@@ -301,11 +306,51 @@ gg_status prepare_gather(const gg_heap *heap, int rank, const void *input, int64
                  (uint64_t)a.bn_b | (uint64_t)a.row_b | 16u;
     const int granule = (int)(g & (~g + 1));  // lowest set bit, <= 16
     const bool bulk_ok = granule == 16;
+    // tensor maps: 16-byte aligned bases and pitches, a box of at most 256 x 256
+    // elements whose rows are whole 16-byte units (N itself may be ragged)
+    const bool tma_ok = ((in_align | (uint64_t)out_off | (uint64_t)a.ld_in_b |
+                          (uint64_t)a.ld_out_b | (uint64_t)a.bn_b) % 16 == 0) &&
+                        tile.block_n <= 256 && tile.block_m <= 256;
     if (path == GG_AG_BULK && !bulk_ok)
         return fail(GG_ERR_ALIGNMENT,
                     "bulk path needs 16-byte aligned input, output, pitches, block_n and N "
                     "(in bytes)");
-    *vec_bytes = (path == GG_AG_BULK || (path == GG_AG_AUTO && bulk_ok)) ? 0 : granule;
+    if (path == GG_AG_TMA && !tma_ok)
+        return fail(GG_ERR_ALIGNMENT,
+                    "tensor-map path needs 16-byte aligned input, output, pitches and "
+                    "block_n*elem_size, and block_n <= 256");
+    int k;
+    if (path == GG_AG_TMA || (path == GG_AG_AUTO && tma_ok))
+        k = kTma;
+    else if (path == GG_AG_BULK || (path == GG_AG_AUTO && bulk_ok))
+        k = kBulk;
+    else
+        k = kVector;
+    *kind = k;
+    *vec_bytes = granule;
+    if (k == kTma && in_map && maps) {
+        const CUtensorMapDataType dt =
+            es == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+        const uint32_t box[3] = {(uint32_t)tile.block_n, (uint32_t)tile.block_m, 1};
+        const uint64_t dims[3] = {(uint64_t)N, (uint64_t)M,
+                                  (uint64_t)(rank == -1 ? heap->H : 1)};
+        const uint64_t strides[2] = {(uint64_t)a.ld_in_b,
+                                     rank == -1 ? (uint64_t)heap->part
+                                                : (uint64_t)(M * a.ld_in_b)};
+        const void *ibase = rank == -1 ? reinterpret_cast<const void *>(heap->base + a.in_off)
+                                       : input;
+        if (!gg::encode_map(in_map, dt, 3, ibase, dims, strides, box,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
+            return fail(GG_ERR_CUDA, "encoding the input tensor map");
+        uint64_t member_out[GG_MAX_WORLD];
+        for (int q = 0; q < W; ++q)
+            member_out[q] = heap->host_bases[group.rank_start + q * group.rank_stride] +
+                            (uint64_t)out_off;
+        if (!gg::encode_out_maps(maps, member_out, W, M, N, a.ld_out_b, es,
+                                 (uint32_t)tile.block_n, (uint32_t)tile.block_m, dt,
+                                 CU_TENSOR_MAP_SWIZZLE_NONE))
+            return fail(GG_ERR_CUDA, "encoding the output tensor maps");
+    }
     *out_args = a;
     *launch = true;
     return ok();
@@ -321,15 +366,23 @@ gg_status gg_all_gather_path(const gg_heap *heap, int rank, const void *input, i
                              gg_stream_t stream, gg_ag_path path)
 {
     gg::GatherArgs a;
-    int vec = 0;
+    int kind = kVector, vec = 0;
     bool launch = false;
+    static thread_local CUtensorMap in_map;
+    static thread_local gg::OutMaps maps;
     gg_status st = prepare_gather(heap, rank, input, ld_in, output, ld_out, M, N, dtype, tile,
-                                  comm_programs, group, dev_status, path, &a, &vec, &launch);
+                                  comm_programs, group, dev_status, path, &a, &kind, &vec,
+                                  &in_map, &maps, &launch);
     if (st != GG_OK || !launch)
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = vec == 0 ? gg::launch_gather_bulk(a, comm_programs, s)
-                             : gg::launch_gather_vec(a, comm_programs, vec, s);
+    cudaError_t e;
+    if (kind == kTma)
+        e = gg::launch_gather_tma(in_map, maps, a, comm_programs, s);
+    else if (kind == kBulk)
+        e = gg::launch_gather_bulk(a, comm_programs, s);
+    else
+        e = gg::launch_gather_vec(a, comm_programs, vec, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "launching the all-gather");
     return ok();
@@ -341,12 +394,14 @@ gg_status gg_all_gather_check(const gg_heap *heap, int rank, const void *input, 
                               gg_ag_path *chosen)
 {
     gg::GatherArgs a;
-    int vec = 0;
+    int kind = kVector, vec = 0;
     bool launch = false;
     gg_status st = prepare_gather(heap, rank, input, ld_in, output, ld_out, M, N, dtype, tile,
-                                  comm_programs, group, nullptr, path, &a, &vec, &launch);
+                                  comm_programs, group, nullptr, path, &a, &kind, &vec, nullptr,
+                                  nullptr, &launch);
     if (chosen)
-        *chosen = !launch ? GG_AG_AUTO : (vec == 0 ? GG_AG_BULK : GG_AG_VECTOR);
+        *chosen = !launch ? GG_AG_AUTO
+                          : (kind == kTma ? GG_AG_TMA : (kind == kBulk ? GG_AG_BULK : GG_AG_VECTOR));
     return st;
 }
 
@@ -366,7 +421,8 @@ namespace {
 gg_status prepare_fused(const gg_heap *heap, int rank, const void *A, int64_t lda, const void *B,
                         int64_t ldb, void *output, int64_t ld_out, int64_t M, int64_t N,
                         int64_t K, gg_dtype dtype, gg_tile tile, int comm_programs,
-                        gg_group group, int *dev_status, gg::FusedArgs *out_args, bool *launch)
+                        gg_group group, int *dev_status, gg::FusedArgs *out_args,
+                        gg::OutMaps *maps, bool *launch)
 {
     *launch = false;
     int gi = -1;
@@ -407,7 +463,6 @@ gg_status prepare_fused(const gg_heap *heap, int rank, const void *A, int64_t ld
         return st;
 
     gg::FusedArgs f{};
-    f.bases = heap->dev_table;
     f.W = W;
     f.rank_start = group.rank_start;
     f.rank_stride = group.rank_stride;
@@ -454,6 +509,18 @@ gg_status prepare_fused(const gg_heap *heap, int rank, const void *A, int64_t ld
         if (overlap(ub, ub + b_ext, o0, o0 + out_ext))
             return fail(GG_ERR_INVALID_ARG, "B overlaps the output of member %d", q);
     }
+    if (maps) {
+        // the per-peer translation, once per launch: member d's output address
+        uint64_t member_out[GG_MAX_WORLD];
+        for (int q = 0; q < W; ++q)
+            member_out[q] = heap->host_bases[group.rank_start + q * group.rank_stride] +
+                            (uint64_t)out_off;
+        const CUtensorMapDataType dt =
+            dtype == GG_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        if (!gg::encode_out_maps(maps, member_out, W, M, N, ld_out * 2, 2, 64, 32, dt,
+                                 CU_TENSOR_MAP_SWIZZLE_128B))
+            return fail(GG_ERR_CUDA, "encoding the output tensor maps");
+    }
     *out_args = f;
     *launch = true;
     return ok();
@@ -474,13 +541,14 @@ gg_status gg_matmul_all_gather_path(const gg_heap *heap, int rank, const void *A
     if (path == GG_MAG_2SM && comm_programs < 2)
         return fail(GG_ERR_INVALID_ARG, "the 2-SM path needs comm_programs >= 2 (one CTA pair)");
     gg::FusedArgs f;
+    static thread_local gg::OutMaps maps;
     bool launch = false;
     gg_status st = prepare_fused(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype, tile,
-                                 comm_programs, group, dev_status, &f, &launch);
+                                 comm_programs, group, dev_status, &f, &maps, &launch);
     if (st != GG_OK || !launch)
         return st;
     const char *why = nullptr;
-    cudaError_t e = gg::launch_matmul_all_gather(f, comm_programs, (int)path,
+    cudaError_t e = gg::launch_matmul_all_gather(f, maps, comm_programs, (int)path,
                                                  reinterpret_cast<cudaStream_t>(stream), &why);
     if (e != cudaSuccess)
         return why ? fail(GG_ERR_CUDA, "%s: %s", why, cudaGetErrorName(e))
@@ -506,7 +574,7 @@ gg_status gg_matmul_all_gather_check(const gg_heap *heap, int rank, const void *
     gg::FusedArgs f;
     bool launch = false;
     return prepare_fused(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype, tile,
-                         comm_programs, group, nullptr, &f, &launch);
+                         comm_programs, group, nullptr, &f, nullptr, &launch);
 }
 
 gg_status gg_set_wait_limit_ns(uint64_t ns)

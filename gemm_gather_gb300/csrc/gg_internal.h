@@ -1,5 +1,6 @@
 // Declarations shared by the library's translation units (host side).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -8,6 +9,23 @@ namespace gg {
 
 constexpr int kMaxWorld = 64;
 constexpr int kStatusTimeout = -6;  // GG_ERR_TIMEOUT
+
+// One TMA tensor map per group member's gathered output (kernel parameter).
+struct OutMaps {
+    CUtensorMap map[kMaxWorld];
+};
+
+bool tensor_maps_available();
+// A tiled tensor map of `rank` dimensions (dims in elements, strides in bytes
+// for dimensions 1..rank-1, box in elements), no interleave, zero OOB fill.
+bool encode_map(CUtensorMap *map, CUtensorMapDataType dt, int rank, const void *base,
+                const uint64_t *dims, const uint64_t *strides_b, const uint32_t *box,
+                CUtensorMapSwizzle swizzle);
+// Output maps of W members: member d's output at member_out[d], viewed as
+// {N, M, W} so that boxes clip at the end of each row block.
+bool encode_out_maps(OutMaps *out, const uint64_t *member_out, int W, int64_t M, int64_t N,
+                     int64_t ld_out_b, int es, uint32_t box_cols, uint32_t box_rows,
+                     CUtensorMapDataType dt, CUtensorMapSwizzle swizzle);
 
 // One launch of the tiled all-gather.  A "source" is a group member whose
 // M x N block is gathered; a launch covers n_src consecutive group indices
@@ -26,6 +44,7 @@ struct GatherArgs {
     int bm;                     // tile rows
     int64_t bn_b;               // tile row bytes (block_n * element size)
     int64_t tiles_n, tiles_per_src, total_items;
+    int es;                     // element size (bytes)
     int *status;
     uint64_t wait_limit_ns;
     int inject_stall;  // test hook: program 0 never arms its first stage
@@ -33,12 +52,16 @@ struct GatherArgs {
 
 // Bulk path: 16-byte aligned addresses, pitches, bn_b and row_b.
 cudaError_t launch_gather_bulk(const GatherArgs &a, int programs, cudaStream_t s);
+// Tensor-map path: in_map views the source blocks as {N, M, heaps} (or the one
+// block as {N, M, 1}); out holds one map per member; box = one tile.
+cudaError_t launch_gather_tma(const CUtensorMap &in_map, const OutMaps &out, const GatherArgs &a,
+                              int programs, cudaStream_t s);
 // Vector path: vec_bytes in {16, 8, 4, 2} divides every address, pitch and row length.
 cudaError_t launch_gather_vec(const GatherArgs &a, int programs, int vec_bytes, cudaStream_t s);
 
-// One launch of the fused matmul + all-gather (see mag_kernel.cu).
+// One launch of the fused matmul + all-gather (see mag_kernel.cu).  The
+// outputs are reached through per-member tensor maps (OutMaps).
 struct FusedArgs {
-    const uint64_t *bases;
     int W, rank_start, rank_stride;
     int n_src, src_first;
     const void *a_abs;     // non-null: the one source's A (any device memory)
@@ -59,7 +82,7 @@ struct FusedArgs {
 };
 
 // variant: 0 = automatic (2-SM pairs when programs >= 2), 1 = 1-SM, 2 = 2-SM
-cudaError_t launch_matmul_all_gather(const FusedArgs &a, int programs, int variant, cudaStream_t s,
-                                     const char **why);
+cudaError_t launch_matmul_all_gather(const FusedArgs &a, const OutMaps &out, int programs,
+                                     int variant, cudaStream_t s, const char **why);
 
 }  // namespace gg

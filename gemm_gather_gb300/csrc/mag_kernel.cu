@@ -11,13 +11,16 @@
 //     from one thread; tcgen05.commit frees ring stages and hands finished
 //     accumulators to the epilogue;
 //   * warps 2-5 (epilogue): tcgen05.ld of their 32 TMEM lanes (= tile rows),
-//     round to f16/bf16, write each row once into a padded shared-memory
-//     staging row, then one bulk copy (cp.async.bulk shared->global) per row
-//     and destination: the local copy first, then the peers in rotated order.
+//     round to f16/bf16 and write each value once into shared memory as
+//     32-row x 64-column boxes in the 128-byte swizzled layout, then one TMA
+//     tensor store (cp.async.bulk.tensor shared->global) per box and
+//     destination: the local copy first, then the peers in rotated order.
 //     The accumulator is released right after it has been read, so the next
 //     tile's MMAs overlap this tile's stores.
-// The W destination bases come from the heap-bases table, loaded once per CTA
-// before any tile (the hoisted translation).
+// Each destination's tensor map is built on the host from the heap-bases
+// table once per launch (the per-peer translation hoisted out of every loop);
+// the map views that member's output as {N, M, W} so that a box is clipped at
+// the end of its own row block.
 //
 // Every mbarrier wait is bounded (wall-clock limit from the launch); a wait
 // that gives up stores GG_ERR_TIMEOUT in the status word, raises a CTA-wide
@@ -27,8 +30,6 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
-
-#include <mutex>
 
 #include "gg_internal.h"
 #include "ptx.cuh"
@@ -43,22 +44,23 @@ constexpr int kThreads = 192;                   // 6 warps
 constexpr int kTmemCols = 512;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
+constexpr int kBox = 32 * 64 * 2;               // 4 KB: one epilogue store box, 32 rows x 64 cols
+
 // Geometry of the 1-SM (CG = 1) and 2-SM (CG = 2) variants.  With CG = 2 a
 // CTA pair computes a 256 x 256 tile: each CTA holds its 128 rows of A and
 // one 128-column half of B; the leader CTA's single thread issues
 // tcgen05.mma.cta_group::2 over both CTAs' shared memory and TMEM.
 template <int CG>
 struct Geo {
-    static constexpr int kStages = CG == 1 ? 3 : 5;
+    static constexpr int kStages = CG == 1 ? 4 : 6;
     static constexpr int kBCols = BN / CG;            // B columns one CTA holds
     static constexpr int kBStage = BK * kBCols * 2;   // 32 KB or 16 KB
     static constexpr int kTileM = BM * CG;            // rows of one (pair) tile
-    // The epilogue stages each row in column passes of kEpiCols; the staged
-    // row pitch adds 16 bytes so 16-byte stores of 8 consecutive rows hit
-    // distinct banks.
-    static constexpr int kEpiCols = CG == 1 ? 256 : 128;
-    static constexpr int kEpiPitch = kEpiCols * 2 + 16;
-    static constexpr int kEpiWarp = 32 * kEpiPitch;   // one epilogue warp's 32 rows
+    // The epilogue stages each warp's 32 rows in column passes of kEpiCols,
+    // as kEpiCols/64 swizzled boxes.
+    static constexpr int kEpiCols = CG == 1 ? 64 : 128;
+    static constexpr int kEpiBoxes = kEpiCols / 64;
+    static constexpr int kEpiWarp = kEpiBoxes * kBox;  // one epilogue warp's staging
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kAStage;
     static constexpr int kOffEpi = kOffB + kStages * kBStage;
@@ -66,12 +68,11 @@ struct Geo {
 };
 
 struct FusedShared {
-    uint64_t full[5];
-    uint64_t empty[5];
+    uint64_t full[6];
+    uint64_t empty[6];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t mma_done;
-    uint64_t dst[kMaxWorld];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -122,6 +123,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// shared -> global tensor store of one box; completion by bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1,
+                                             int c2, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], "
+        "[%1], %5;" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -385,7 +397,7 @@ __device__ __forceinline__ TileCoord tile_coord(const FusedArgs &a, int64_t t, i
 
 template <int CG>
 __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtensorMap &map_b,
-                                         const FusedArgs &a)
+                                         const OutMaps &out, const FusedArgs &a)
 {
     using G = Geo<CG>;
     extern __shared__ uint8_t smem_raw[];
@@ -428,8 +440,8 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
         tmem_alloc<CG>(ptx::smem_addr(&sh.tmem_base));
         tc_fence_before();
     }
-    for (int i = threadIdx.x; i < a.W; i += blockDim.x)
-        sh.dst[i] = a.bases[a.rank_start + i * a.rank_stride] + (uint64_t)a.out_off;
+    if (threadIdx.x < (unsigned)a.W)
+        prefetch_tensormap(&out.map[threadIdx.x]);
     __syncthreads();
     if constexpr (CG == 2)
         cluster_sync();  // the peer's barriers exist before anything signals them
@@ -565,11 +577,12 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
     } else {
         // ===================== epilogue (warps 2-5) =========================
         const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const uint32_t stage_row =
-            base + G::kOffEpi + (uint32_t)(q * G::kEpiWarp + lane * G::kEpiPitch);
+        const uint32_t warp_stage = base + G::kOffEpi + (uint32_t)(q * G::kEpiWarp);
+        const uint32_t my_row = warp_stage + (uint32_t)lane * 128u;  // row `lane` of box 0
+        const uint32_t swz = (uint32_t)(lane & 7);                  // 128-byte swizzle phase
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        const int64_t ld_out_b = a.ld_out * 2;
         const uint64_t pol_c = ptx::policy_evict_first();  // output: written once, never read
+        constexpr int kOps = G::kEpiBoxes;                   // stores per destination per pass
         int64_t lt = 0;
         bool ok = true;
         for (int64_t t = unit; t < total; t += nunits, ++lt) {
@@ -584,33 +597,37 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
             }
             tc_fence_after();
             const uint32_t t_addr = tmem + lane_addr + (uint32_t)(acc * BN);
-            const int64_t row = (int64_t)c.tm * G::kTileM + (int64_t)rank * BM + q * 32 + lane;
-            const int64_t row_off = ((int64_t)c.g * a.M + row) * ld_out_b;
+            // first row of this warp's boxes, within the source's row block
+            const int row0 = c.tm * G::kTileM + (int)rank * BM + q * 32;
 #pragma unroll 1
             for (int pass = 0; pass < BN; pass += G::kEpiCols) {
-                // this thread's staging row is free once its previous stores have read it
+                // the staging boxes are free once this warp's previous stores read them
                 ptx::bulk_wait_read<0>();
+                __syncwarp();
 #pragma unroll 1
-                for (int cb = 0; cb < G::kEpiCols; cb += 64) {
+                for (int b = 0; b < G::kEpiBoxes; ++b) {
                     uint32_t v0[32], v1[32];
-                    tmem_ld_32x32b_x32(t_addr + (uint32_t)(pass + cb), v0);
-                    tmem_ld_32x32b_x32(t_addr + (uint32_t)(pass + cb + 32), v1);
+                    tmem_ld_32x32b_x32(t_addr + (uint32_t)(pass + b * 64), v0);
+                    tmem_ld_32x32b_x32(t_addr + (uint32_t)(pass + b * 64 + 32), v1);
                     tmem_wait_ld(v0);
                     reg_order(v1);
+                    // 16-byte chunk k of the row holds columns 8k..8k+7 and sits at
+                    // chunk position k ^ (row mod 8) (the 128-byte swizzle)
+                    const uint32_t rowp = my_row + (uint32_t)(b * kBox);
 #pragma unroll
-                    for (int j = 0; j < 32; j += 8)
-                        st_shared_v4(stage_row + (uint32_t)(cb * 2 + j * 2),
-                                     pack2(v0[j], v0[j + 1], a.is_bf16),
-                                     pack2(v0[j + 2], v0[j + 3], a.is_bf16),
-                                     pack2(v0[j + 4], v0[j + 5], a.is_bf16),
-                                     pack2(v0[j + 6], v0[j + 7], a.is_bf16));
+                    for (int k = 0; k < 4; ++k)
+                        st_shared_v4(rowp + ((((uint32_t)k) ^ swz) << 4),
+                                     pack2(v0[8 * k], v0[8 * k + 1], a.is_bf16),
+                                     pack2(v0[8 * k + 2], v0[8 * k + 3], a.is_bf16),
+                                     pack2(v0[8 * k + 4], v0[8 * k + 5], a.is_bf16),
+                                     pack2(v0[8 * k + 6], v0[8 * k + 7], a.is_bf16));
 #pragma unroll
-                    for (int j = 0; j < 32; j += 8)
-                        st_shared_v4(stage_row + (uint32_t)((cb + 32) * 2 + j * 2),
-                                     pack2(v1[j], v1[j + 1], a.is_bf16),
-                                     pack2(v1[j + 2], v1[j + 3], a.is_bf16),
-                                     pack2(v1[j + 4], v1[j + 5], a.is_bf16),
-                                     pack2(v1[j + 6], v1[j + 7], a.is_bf16));
+                    for (int k = 0; k < 4; ++k)
+                        st_shared_v4(rowp + ((((uint32_t)(k + 4)) ^ swz) << 4),
+                                     pack2(v1[8 * k], v1[8 * k + 1], a.is_bf16),
+                                     pack2(v1[8 * k + 2], v1[8 * k + 3], a.is_bf16),
+                                     pack2(v1[8 * k + 4], v1[8 * k + 5], a.is_bf16),
+                                     pack2(v1[8 * k + 6], v1[8 * k + 7], a.is_bf16));
                 }
                 if (pass + G::kEpiCols >= BN) {
                     // accumulator fully read: hand it back to the (leader's) MMA warp
@@ -624,18 +641,22 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
                             ptx::mbar_arrive(e);
                     }
                 }
-                // staged row segment -> every destination, local first, peers rotated
+                // staged boxes -> every destination, local first, peers rotated
                 ptx::fence_proxy_async_smem();
-                const int64_t col0 = (int64_t)c.tn * BN + pass;
-                if (row < a.M && col0 < a.N) {
-                    const uint32_t rb = (uint32_t)(gg_min64(G::kEpiCols, a.N - col0) * 2);
-                    const int64_t off = row_off + col0 * 2;
-                    for (int j = 0; j < a.W; ++j) {
+                __syncwarp();
+                const int col0 = c.tn * BN + pass;
+                if (row0 < a.M) {
+                    for (int op = lane; op < a.W * kOps; op += 32) {
+                        const int j = op / kOps;
+                        const int b = op - j * kOps;
+                        const int col = col0 + b * 64;
+                        if (col >= a.N)
+                            continue;
                         int i = c.g + j;
                         if (i >= a.W)
                             i -= a.W;
-                        ptx::bulk_s2g_hint(reinterpret_cast<uint8_t *>(sh.dst[i]) + off, stage_row,
-                                           rb, pol_c);
+                        tma_store_3d(&out.map[i], warp_stage + (uint32_t)(b * kBox), col, row0, c.g,
+                                     pol_c);
                     }
                 }
                 ptx::bulk_commit();
@@ -661,46 +682,24 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
 
 __global__ void __launch_bounds__(kThreads, 1)
     mag1_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                const FusedArgs a)
+                const __grid_constant__ OutMaps out, const FusedArgs a)
 {
-    mag_body<1>(map_a, map_b, a);
+    mag_body<1>(map_a, map_b, out, a);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mag2_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                const FusedArgs a)
+                const __grid_constant__ OutMaps out, const FusedArgs a)
 {
-    mag_body<2>(map_a, map_b, a);
-}
-
-// ---- host: tensor maps and launch ------------------------------------------------
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn()
-{
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
+    mag_body<2>(map_a, map_b, out, a);
 }
 
 }  // namespace
 
-cudaError_t launch_matmul_all_gather(const FusedArgs &a, int programs, int variant, cudaStream_t s,
-                                     const char **why)
+cudaError_t launch_matmul_all_gather(const FusedArgs &a, const OutMaps &out, int programs,
+                                     int variant, cudaStream_t s, const char **why)
 {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) {
+    if (!tensor_maps_available()) {
         *why = "cuTensorMapEncodeTiled is not available";
         return cudaErrorNotSupported;
     }
@@ -710,31 +709,23 @@ cudaError_t launch_matmul_all_gather(const FusedArgs &a, int programs, int varia
     {
         // A as {K, M, heaps}: one partition per heap (group launch) or the one block
         const bool group = a.a_abs == nullptr;
-        void *ga = group ? reinterpret_cast<void *>(a.heap_base + (uint64_t)a.a_off)
-                         : const_cast<void *>(a.a_abs);
-        const cuuint64_t dims[3] = {(cuuint64_t)a.K, (cuuint64_t)a.M,
-                                    (cuuint64_t)(group ? a.num_heaps : 1)};
-        const cuuint64_t strides[2] = {(cuuint64_t)a.lda * 2,
-                                       group ? (cuuint64_t)a.part_bytes
-                                             : (cuuint64_t)(a.M * a.lda * 2)};
-        const cuuint32_t box[3] = {BK, BM, 1};
-        const cuuint32_t estr[3] = {1, 1, 1};
-        if (enc(&map_a, dt, 3, ga, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
+        const void *ga = group ? reinterpret_cast<const void *>(a.heap_base + (uint64_t)a.a_off)
+                               : a.a_abs;
+        const uint64_t dims[3] = {(uint64_t)a.K, (uint64_t)a.M,
+                                  (uint64_t)(group ? a.num_heaps : 1)};
+        const uint64_t strides[2] = {(uint64_t)a.lda * 2,
+                                     group ? a.part_bytes : (uint64_t)(a.M * a.lda * 2)};
+        const uint32_t box[3] = {BK, BM, 1};
+        if (!encode_map(&map_a, dt, 3, ga, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) {
             *why = "encoding the tensor map of A";
             return cudaErrorInvalidValue;
         }
     }
     {
-        const cuuint64_t dims[2] = {(cuuint64_t)a.N, (cuuint64_t)a.K};
-        const cuuint64_t strides[1] = {(cuuint64_t)a.ldb * 2};
-        const cuuint32_t box[2] = {64, BK};
-        const cuuint32_t estr[2] = {1, 1};
-        if (enc(&map_b, dt, 2, const_cast<void *>(a.b), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-            CUDA_SUCCESS) {
+        const uint64_t dims[2] = {(uint64_t)a.N, (uint64_t)a.K};
+        const uint64_t strides[1] = {(uint64_t)a.ldb * 2};
+        const uint32_t box[2] = {64, BK};
+        if (!encode_map(&map_b, dt, 2, a.b, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) {
             *why = "encoding the tensor map of B";
             return cudaErrorInvalidValue;
         }
@@ -772,7 +763,7 @@ cudaError_t launch_matmul_all_gather(const FusedArgs &a, int programs, int varia
         int64_t clusters = gg_min64(programs / 2, pairs);
         if (resident > 0)
             clusters = gg_min64(clusters, resident);
-        mag2_kernel<<<(int)(2 * clusters), kThreads, smem_bytes<2>(), s>>>(map_a, map_b, a);
+        mag2_kernel<<<(int)(2 * clusters), kThreads, smem_bytes<2>(), s>>>(map_a, map_b, out, a);
     } else {
         const int64_t tiles = (int64_t)a.n_src * ((a.M + BM - 1) / BM) * tiles_n;
         e = cudaFuncSetAttribute(mag1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -782,7 +773,7 @@ cudaError_t launch_matmul_all_gather(const FusedArgs &a, int programs, int varia
             return e;
         }
         mag1_kernel<<<(int)gg_min64(programs, tiles), kThreads, smem_bytes<1>(), s>>>(map_a, map_b,
-                                                                                    a);
+                                                                                    out, a);
     }
     return cudaGetLastError();
 }

@@ -130,7 +130,8 @@ gg_status gg_heap_destroy(gg_heap *heap);
  *   up, GG_ERR_TIMEOUT is stored there (first error wins; the caller zeroes
  *   it).  M == 0 or N == 0 launches nothing and returns GG_OK.
  * Any alignment is accepted: 16-byte aligned pointers and pitches take the
- *   bulk-copy path, others a narrower vector path.  Results are identical.
+ *   tensor-map or bulk-copy path, others a narrower vector path.  Results
+ *   are identical.
  * ------------------------------------------------------------------------- */
 gg_status gg_all_gather(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
                         void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
@@ -138,7 +139,13 @@ gg_status gg_all_gather(const gg_heap *heap, int rank, const void *input, int64_
                         gg_stream_t stream);
 
 /* Data-path variants of gg_all_gather (same arguments and result):
- *   GG_AG_AUTO      bulk path when aligned, else vector path (gg_all_gather)
+ *   GG_AG_AUTO      tensor-map path when it applies, else bulk, else vector
+ *                   (what gg_all_gather does)
+ *   GG_AG_TMA       each tile moved by one TMA tensor load into shared memory
+ *                   and one TMA tensor store per destination, through tensor
+ *                   maps built on the host from the heap-bases table; needs
+ *                   16-byte aligned input, output, pitches and
+ *                   block_n*elem_size, and block_n <= 256 (N may be ragged)
  *   GG_AG_BULK      tiles staged in shared memory by bulk copies (TMA engine),
  *                   stored to each destination by bulk copies; needs 16-byte
  *                   aligned pointers, pitches, block_n*elem_size and
@@ -146,7 +153,7 @@ gg_status gg_all_gather(const gg_heap *heap, int rank, const void *input, int64_
  *   GG_AG_VECTOR    16/8/4/2-byte vector loads into registers, then one vector
  *                   store per destination (widest width the alignment allows)
  */
-typedef enum { GG_AG_AUTO = 0, GG_AG_BULK = 1, GG_AG_VECTOR = 2 } gg_ag_path;
+typedef enum { GG_AG_AUTO = 0, GG_AG_BULK = 1, GG_AG_VECTOR = 2, GG_AG_TMA = 3 } gg_ag_path;
 
 gg_status gg_all_gather_path(const gg_heap *heap, int rank, const void *input,
                              int64_t ld_in, void *output, int64_t ld_out, int64_t M,
@@ -156,7 +163,8 @@ gg_status gg_all_gather_path(const gg_heap *heap, int rank, const void *input,
 
 /* Validate a gg_all_gather_path call exactly as the launching call does and
  * launch nothing.  *chosen (nullable) receives the path a launch would take
- * (GG_AG_BULK or GG_AG_VECTOR; GG_AG_AUTO when there is nothing to launch). */
+ * (GG_AG_TMA, GG_AG_BULK or GG_AG_VECTOR; GG_AG_AUTO when there is nothing
+ * to launch). */
 gg_status gg_all_gather_check(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
                               void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
                               gg_tile tile, int comm_programs, gg_group group, gg_ag_path path,

@@ -71,16 +71,24 @@ def ag(heap, **kw):
 
 
 def test_gather_valid_calls(heap):
-    assert ag(heap) == "bulk"
-    assert ag(heap, rank=1) == "bulk"
+    assert ag(heap) == "tma"
+    assert ag(heap, rank=1) == "tma"
+    assert ag(heap, path="bulk") == "bulk"
+    assert ag(heap, path="tma") == "tma"
     assert ag(heap, M=0) == "none"
     assert ag(heap, N=0) == "none"
     assert ag(heap, input=BASE + 4098) == "vector"
     assert ag(heap, path="vector") == "vector"
-    assert ag(heap, group=(1, 2, 4), rank=5) == "bulk"
-    assert ag(heap, N=255, ld_in=256, ld_out=256) == "vector"
+    assert ag(heap, group=(1, 2, 4), rank=5) == "tma"
+    # a ragged N with 16-byte pitches still takes tensor maps (boxes clip); bulk
+    # copies need whole 16-byte rows
+    assert ag(heap, N=255, ld_in=256, ld_out=256) == "tma"
+    assert ag(heap, N=255, ld_in=256, ld_out=256, path="auto", tile=(8, 264)) == "vector"
+    # block_n above 256 elements is beyond a tensor-map box: bulk copies instead
+    assert ag(heap, tile=(4, 512), N=1024, ld_in=1024, ld_out=1024,
+              output=BASE + (4 << 20)) == "bulk"
     # an explicit 32x64 tile is accepted as given (never remapped)
-    assert ag(heap, tile=(32, 64)) == "bulk"
+    assert ag(heap, tile=(32, 64)) == "tma"
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -107,6 +115,9 @@ def test_gather_valid_calls(heap):
     (dict(input=BASE + (1 << 20) + 512), _lib.GG_ERR_INVALID_ARG),  # overlaps the output
     (dict(rank=0, input=BASE + PART + (1 << 20)), _lib.GG_ERR_INVALID_ARG),  # overlaps member 1
     (dict(input=BASE + 4098, path="bulk"), _lib.GG_ERR_ALIGNMENT),
+    (dict(input=BASE + 4098, path="tma"), _lib.GG_ERR_ALIGNMENT),
+    (dict(tile=(4, 512), N=1024, ld_in=1024, ld_out=1024, output=BASE + (4 << 20),
+          path="tma"), _lib.GG_ERR_ALIGNMENT),
     (dict(dtype=7), _lib.GG_ERR_INVALID_ARG),
     (dict(output=0), _lib.GG_ERR_INVALID_ARG),
 ])
@@ -173,8 +184,8 @@ def test_page_facts_tile_geometry():
         assert t["block_n"] * es == t["row_bytes"]
     heap = gg.heap_wrap(BASE, PART, 8, TABLE)
     t = facts["explicit_tile_not_remapped"]
-    # accepted as the 32x64 tile it is: the bulk path needs block_n*2 % 16 == 0 (128 B rows)
-    assert ag(heap, tile=(t["block_m"], t["block_n"])) == "bulk"
+    # accepted as the 32x64 tile it is (128-byte rows: a tensor-map box of 32 x 64)
+    assert ag(heap, tile=(t["block_m"], t["block_n"])) == "tma"
     s = facts["sweep"]
     assert len(s["M"]) * len(s["N"]) * len(s["dtypes"]) * len(s["comm_sms"]) == s["configurations"]
     p = facts["peers_per_tile"]

@@ -81,21 +81,27 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("path", ["auto", "bulk", "vector"])
+@pytest.mark.parametrize("path", ["auto", "tma", "bulk", "vector"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"H{c[0]}g{c[1]}_{c[2]}x{c[3]}e{c[4]}t{c[5]}p{c[6]}")
 def test_group_launch_matches_oracle(oracle, case, path):
     H, group, M, N, es, tile, programs, pi, po = case
-    bulk_ok = (N * es) % 16 == 0 and (tile[1] * es) % 16 == 0 and ((N + pi) * es) % 16 == 0 \
-        and ((N + po) * es) % 16 == 0
-    if path == "bulk" and not bulk_ok:
+    pitches_ok = ((N + pi) * es) % 16 == 0 and ((N + po) * es) % 16 == 0 \
+        and (tile[1] * es) % 16 == 0
+    if path == "bulk" and not (pitches_ok and (N * es) % 16 == 0):
         pytest.skip("bulk path needs 16-byte rows and tiles")
+    if path == "tma" and not (pitches_ok and tile[1] <= 256):
+        pytest.skip("tensor-map path needs 16-byte pitches and tile rows")
     _run_case(oracle, H, group, M, N, es, tile, programs, pi, po, path=path)
 
 
+@pytest.mark.parametrize("path", ["auto", "bulk"])
 @pytest.mark.parametrize("case", CASES[:8], ids=lambda c: f"H{c[0]}g{c[1]}_{c[2]}x{c[3]}")
-def test_single_rank_launches_match_oracle(oracle, case):
+def test_single_rank_launches_match_oracle(oracle, case, path):
     H, group, M, N, es, tile, programs, pi, po = case
-    _run_case(oracle, H, group, M, N, es, tile, programs, pi, po, mode="ranks")
+    if path == "bulk" and not (((N + pi) * es) % 16 == 0 and ((N + po) * es) % 16 == 0
+                               and (tile[1] * es) % 16 == 0 and (N * es) % 16 == 0):
+        pytest.skip("bulk path needs 16-byte rows and tiles")
+    _run_case(oracle, H, group, M, N, es, tile, programs, pi, po, mode="ranks", path=path)
 
 
 @pytest.mark.parametrize("case", CASES[:4], ids=lambda c: f"H{c[0]}g{c[1]}_{c[2]}x{c[3]}")

@@ -36,14 +36,15 @@ def _gather_heap():
     return lay, host
 
 
-def test_gather_wait_limit_reports_timeout(oracle, short_waits):
+@pytest.mark.parametrize("path", ["bulk", "tma"])
+def test_gather_wait_limit_reports_timeout(oracle, short_waits, path):
     import gemm_gather_gb300 as gg
     lay, host = _gather_heap()
     sh = device_heap(lay, host)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     gg.all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), lay.ld_in, sh.ptr(0, lay.out_off),
                   lay.ld_out, lay.M, lay.N, torch.float16, (8, 256), 4, (0, 1, 4),
-                  status=status, path="bulk")
+                  status=status, path=path)
     torch.cuda.synchronize()
     assert int(status.item()) == TIMEOUT
     # the context is intact: a normal launch gives the oracle's heap
@@ -52,7 +53,7 @@ def test_gather_wait_limit_reports_timeout(oracle, short_waits):
     status.zero_()
     gg.all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), lay.ld_in, sh.ptr(0, lay.out_off),
                   lay.ld_out, lay.M, lay.N, torch.float16, (8, 256), 4, (0, 1, 4),
-                  status=status, path="bulk")
+                  status=status, path=path)
     got = download(sh)
     assert int(status.item()) == 0
     oracle.all_gather(host, lay.part_bytes, lay.in_off, lay.ld_in, lay.out_off, lay.ld_out,
