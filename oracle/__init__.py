@@ -53,6 +53,9 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_all_gather.argtypes = [vp, vp, i64, i32, i64, i64, i64, i64, i64,
                                       i64, i32, i32, i32, i32]
     lib.oracle_all_gather.restype = i32
+    lib.oracle_all_to_all.argtypes = [vp, vp, i64, i32, i64, i64, i64, i64, i64,
+                                      i64, i32, i32, i32, i32]
+    lib.oracle_all_to_all.restype = i32
     lib.oracle_decode16.argtypes = [ctypes.c_uint16, i32]
     lib.oracle_decode16.restype = ctypes.c_double
     lib.oracle_encode16.argtypes = [ctypes.c_double, i32]
@@ -119,6 +122,20 @@ class Oracle:
                                         M, N, esize, *group)
         if rc:
             raise ValueError("oracle_all_gather rejected its arguments")
+
+    # -- all-to-all (iris #594 "Compiler inspection and grouping") ----------
+    def all_to_all(self, heap: np.ndarray, part_bytes: int, in_off: int, ld_in: int,
+                   out_off: int, ld_out: int, M: int, N: int, esize: int,
+                   group: tuple[int, int, int]) -> None:
+        """Member d's output row block i = member i's input row block d (each
+        input is W*M x N); updates ``heap`` in place."""
+        assert heap.dtype == np.uint8 and heap.flags.c_contiguous
+        H = heap.size // part_bytes
+        snapshot = heap.copy()
+        rc = self.lib.oracle_all_to_all(heap.ctypes.data, snapshot.ctypes.data, part_bytes, H,
+                                        in_off, ld_in, out_off, ld_out, M, N, esize, *group)
+        if rc:
+            raise ValueError("oracle_all_to_all rejected its arguments")
 
     # -- 16-bit formats -------------------------------------------------------
     def decode16(self, bits: int, fmt: int) -> float:

@@ -23,6 +23,7 @@
  *    world_size; heap_bases gives each rank's partition.
  *
  * Parity pins (tests/test_oracle_pins.py): index-coded brute force,
+ * all_to_all applied twice is the identity,
  * invariants, torch.distributed gloo all_gather_into_tensor, numpy float64
  * matmul, integer-exact products, one-hot/identity/ones closed forms, numpy
  * float16 and torch bfloat16 conversions.  No function here is unpinned.
@@ -106,6 +107,44 @@ int oracle_all_gather(uint8_t *heap, const uint8_t *src_heap, int64_t part_bytes
                                             world_size, r);
         if (rc)
             return rc;
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * All-to-all (iris #594, "Compiler inspection and grouping", and iris #591
+ * Work: the Gluon all_to_all over the same symmetric heap).  Each member i
+ * holds W blocks of M x N rows (block d at rows d*M..d*M+M-1 of its W*M x N
+ * input, pitch ld_in, at in_off); block d is meant for member d.  The output
+ * of member d (W*M x N, pitch ld_out, at out_off) holds, in row block i, the
+ * block member i meant for d:
+ *     out_d[(i*M + m), n] = in_i[(d*M + m), n]
+ * -- torch.distributed.all_to_all_single with equal splits.  Sources are read
+ * from the snapshot src_heap; bytes are copied unchanged; nothing else changes.
+ * ------------------------------------------------------------------------- */
+int oracle_all_to_all(uint8_t *heap, const uint8_t *src_heap, int64_t part_bytes,
+                      int H, int64_t in_off, int64_t ld_in, int64_t out_off,
+                      int64_t ld_out, int64_t M, int64_t N, int esize,
+                      int rank_start, int rank_stride, int world_size)
+{
+    for (int i = 0; i < world_size; ++i) {
+        int src = rank_start + i * rank_stride;
+        for (int d = 0; d < world_size; ++d) {
+            int dst = rank_start + d * rank_stride;
+            if (src < 0 || src >= H || dst < 0 || dst >= H)
+                return -1;
+            const uint8_t *in = src_heap + (int64_t)src * part_bytes + in_off;
+            uint8_t *out = heap + (int64_t)dst * part_bytes + out_off;
+            for (int64_t m = 0; m < M; ++m) {
+                for (int64_t n = 0; n < N; ++n) {
+                    int64_t from = ((d * M + m) * ld_in + n) * esize;
+                    int64_t to = ((i * M + m) * ld_out + n) * esize;
+                    if (in_off + from + esize > part_bytes || out_off + to + esize > part_bytes)
+                        return -1;
+                    memcpy(out + to, in + from, (size_t)esize);
+                }
+            }
+        }
     }
     return 0;
 }

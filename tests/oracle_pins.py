@@ -139,6 +139,85 @@ def pin_gather_w1_copy(o) -> None:
 
 
 # --------------------------------------------------------------------------- #
+# all-to-all                                                                  #
+# --------------------------------------------------------------------------- #
+
+A2A_CASES = [
+    # (H, group, M, N, ld_in pad, ld_out pad)
+    (1, (0, 1, 1), 3, 5, 0, 0),
+    (2, (0, 1, 2), 4, 7, 1, 3),
+    (3, (0, 1, 3), 5, 16, 0, 2),
+    (8, (1, 2, 4), 6, 9, 2, 0),
+    (6, (2, 1, 3), 1, 1, 0, 1),
+]
+
+
+def _a2a_setup(H, group, M, N, pi, po):
+    W = group[2]
+    # input W*M x N per member; the output has the same shape
+    lay = hi.make_layout(H, W, W * M, N, 4, ld_in=N + pi, ld_out=N + po)
+    heap = hi.sentinel_heap(lay)
+    for h in _members(group):
+        blk = gg_inputs.index_packed(h, W * M, N, 4).numpy()
+        hi.put_block(heap, lay, h, blk, lay.in_off, lay.ld_in)
+    return lay, heap
+
+
+def pin_all_to_all_packed(o) -> None:
+    """out_d row block i = member i's input row block d, decoded element by element."""
+    for (H, group, M, N, pi, po) in A2A_CASES:
+        lay, heap = _a2a_setup(H, group, M, N, pi, po)
+        W = group[2]
+        members = _members(group)
+        before = heap.copy()
+        o.all_to_all(heap, lay.part_bytes, lay.in_off, lay.ld_in, lay.out_off, lay.ld_out, M, N,
+                     4, group)
+        for di, d in enumerate(members):
+            out = hi.get_block(heap, lay, d, lay.out_off, W * M, lay.ld_out, N, np.int32)
+            for i in range(W):
+                r, m, n = gg_inputs.index_packed_decode(torch.from_numpy(out[i * M:(i + 1) * M]), 4)
+                assert bool((r == members[i]).all()), ("rank", d, i)
+                assert bool((m == di * M + torch.arange(M).view(M, 1)).all()), ("row", d, i)
+                assert bool((n == torch.arange(N).view(1, N)).all()), ("col", d, i)
+        # only the W*M x N outputs of the members change
+        mask = np.zeros(lay.H * lay.part_bytes, dtype=bool)
+        for d in members:
+            base = d * lay.part_bytes + lay.out_off
+            for rr in range(W * M):
+                s0 = base + rr * lay.ld_out * 4
+                mask[s0: s0 + N * 4] = True
+        assert np.array_equal(heap[~mask], before[~mask])
+
+
+def pin_all_to_all_twice_is_identity(o) -> None:
+    """Exchanging twice returns every member's original blocks (an involution)."""
+    rng = np.random.default_rng(3)
+    for (H, group, M, N) in [(4, (0, 1, 4), 3, 6), (7, (1, 3, 2), 2, 5), (3, (0, 1, 3), 1, 2)]:
+        W = group[2]
+        lay = hi.make_layout(H, W, W * M, N, 2)
+        heap = hi.sentinel_heap(lay)
+        orig = {}
+        for h in _members(group):
+            orig[h] = rng.integers(-30000, 30000, size=(W * M, N)).astype(np.int16)
+            hi.put_block(heap, lay, h, orig[h], lay.in_off, N)
+        o.all_to_all(heap, lay.part_bytes, lay.in_off, N, lay.out_off, N, M, N, 2, group)
+        # second exchange: the outputs become the inputs
+        o.all_to_all(heap, lay.part_bytes, lay.out_off, N, lay.in_off, N, M, N, 2, group)
+        for h in _members(group):
+            back = hi.get_block(heap, lay, h, lay.in_off, W * M, N, N, np.int16)
+            assert np.array_equal(back, orig[h]), h
+
+
+def pin_all_to_all_w1_copy(o) -> None:
+    lay = hi.make_layout(2, 1, 5, 7, 4, ld_in=9, ld_out=8)
+    heap = hi.sentinel_heap(lay)
+    blk = np.arange(35, dtype=np.int32).reshape(5, 7) * 7919
+    hi.put_block(heap, lay, 1, blk, lay.in_off, 9)
+    o.all_to_all(heap, lay.part_bytes, lay.in_off, 9, lay.out_off, 8, 5, 7, 4, (1, 1, 1))
+    assert np.array_equal(hi.get_block(heap, lay, 1, lay.out_off, 5, 8, 7, np.int32), blk)
+
+
+# --------------------------------------------------------------------------- #
 # 16-bit formats                                                              #
 # --------------------------------------------------------------------------- #
 
@@ -296,6 +375,9 @@ ALL_PINS = [
     pin_gather_packed,
     pin_gather_single_contribution,
     pin_gather_w1_copy,
+    pin_all_to_all_packed,
+    pin_all_to_all_twice_is_identity,
+    pin_all_to_all_w1_copy,
     pin_decode16,
     pin_encode16,
     pin_matmul_numpy,

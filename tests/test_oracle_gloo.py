@@ -1,7 +1,8 @@
 """The oracle's all-gather against torch.distributed.all_gather_into_tensor on
 W CPU processes over gloo (the library routine the pages' own tests compare
 with: iris #594 "Multi-GPU CI" and "Local validation"), for a contiguous group
-and a strided subgroup.  CPU only; no GPU is touched."""
+and a strided subgroup, and its all-to-all with all_to_all_single.  CPU only;
+no GPU is touched."""
 import os
 import socket
 
@@ -34,6 +35,11 @@ def _worker(rank, world, port, M, N, sub_ranks, out_dir):
         out = torch.empty((world * M, N), dtype=torch.float32)
         dist.all_gather_into_tensor(out, x)
         np.save(os.path.join(out_dir, f"full_{rank}.npy"), out.numpy())
+        # all_to_all_single with equal splits: rank r's input is W blocks
+        xa = torch.cat([_block(100 * rank + j, M, N) for j in range(world)])
+        oa = torch.empty_like(xa)
+        dist.all_to_all_single(oa, xa)
+        np.save(os.path.join(out_dir, f"a2a_{rank}.npy"), oa.numpy())
         grp = dist.new_group(ranks=sub_ranks)
         if rank in sub_ranks:
             o2 = torch.empty((len(sub_ranks) * M, N), dtype=torch.float32)
@@ -59,6 +65,18 @@ def test_oracle_matches_gloo_all_gather(oracle, tmp_path, world, M, N, sub):
                       M, N, 4, (0, 1, world))
     for h in range(world):
         ref = np.load(tmp_path / f"full_{h}.npy")
+        got = hi.get_block(heap, lay, h, lay.out_off, world * M, lay.ld_out, N, np.float32)
+        assert got.tobytes() == ref.tobytes()
+    # all-to-all with equal splits
+    lay = hi.make_layout(world, world, world * M, N, 4)
+    heap = hi.sentinel_heap(lay)
+    for h in range(world):
+        xa = torch.cat([_block(100 * h + j, M, N) for j in range(world)]).numpy()
+        hi.put_block(heap, lay, h, xa, lay.in_off, lay.ld_in)
+    oracle.all_to_all(heap, lay.part_bytes, lay.in_off, lay.ld_in, lay.out_off, lay.ld_out, M, N,
+                      4, (0, 1, world))
+    for h in range(world):
+        ref = np.load(tmp_path / f"a2a_{h}.npy")
         got = hi.get_block(heap, lay, h, lay.out_off, world * M, lay.ld_out, N, np.float32)
         assert got.tobytes() == ref.tobytes()
     # strided subgroup

@@ -17,7 +17,8 @@ from tests.oracle_pins import ALL_PINS
 SRC = os.path.join(os.path.dirname(oracle_mod.__file__), "gg_oracle.c")
 
 MUTANTS = {
-    "block_index_by_destination": ("((i * M + m) * ld_out + n)", "((q * M + m) * ld_out + n)"),
+    "block_index_by_destination": ("int64_t dst = out_off + ((i * M + m) * ld_out + n) * esize;",
+                                   "int64_t dst = out_off + ((q * M + m) * ld_out + n) * esize;"),
     "columns_reversed": ("src + (m * ld_in + n) * esize", "src + (m * ld_in + (N - 1 - n)) * esize"),
     "local_copy_skipped": ("for (int q = 0; q < world_size; ++q)", "for (int q = 1; q < world_size; ++q)"),
     "member_off_by_one": ("if (rank_start + i * rank_stride == h)", "if (rank_start + i * rank_stride == h + 1)"),
@@ -27,6 +28,10 @@ MUTANTS = {
     "wrong_sign_sum": ("s += a[k] * b[k];", "s -= a[k] * b[k];"),
     "b_transposed_pitch": ("bt[n * K + k] = oracle_decode16(B[k * ldb + n], fmt);",
                            "bt[n * K + k] = oracle_decode16(B[(k % N) * ldb + (n % K)], fmt);"),
+    "a2a_source_block_swapped": ("int64_t from = ((d * M + m) * ld_in + n) * esize;",
+                                 "int64_t from = ((i * M + m) * ld_in + n) * esize;"),
+    "a2a_dest_block_swapped": ("int64_t to = ((i * M + m) * ld_out + n) * esize;",
+                               "int64_t to = ((d * M + m) * ld_out + n) * esize;"),
     "b_column_shifted": ("B[k * ldb + n]", "B[k * ldb + (n + 1) % N]"),
     "a_row_shifted": ("A[m * lda + k]", "A[((m + 1) % M) * lda + k]"),
     "decode_bias_off_by_one": ("v = ldexp((double)((1 << mbits) + f), e - bias - mbits);",
