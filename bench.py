@@ -47,6 +47,8 @@ class GatherCfg:
     stride: int = 1
     values: str = "uniform"  # uniform[-1,1] or normal(0,1)
     path: str = "auto"  # auto / tma / bulk / vector
+    kind: str = "all_gather"  # all_gather / partitioned / all_to_all
+    dests_per_wait: int = 0   # destination grouping (0: all destinations at once)
 
     @property
     def es(self) -> int:
@@ -59,8 +61,9 @@ class GatherCfg:
         grp = "" if (self.start, self.stride) == (0, 1) else \
             f" group(start={self.start},stride={self.stride})"
         kern = "" if self.path == "auto" else f" {self.path}"
-        return (f"all_gather W={self.W} {self.M}x{self.N} {self.dtype} tile {self.bm}x{self.bn} "
-                f"{self.programs} programs{grp}{kern}")
+        grouping = f" {self.dests_per_wait} dests/wait" if self.dests_per_wait else ""
+        return (f"{self.kind} W={self.W} {self.M}x{self.N} {self.dtype} tile {self.bm}x{self.bn} "
+                f"{self.programs} programs{grp}{grouping}{kern}")
 
 
 @dataclass
@@ -107,7 +110,7 @@ def parse_cfg(text: str, base):
             cfg.bm, cfg.bn = (int(x) for x in v.split("x"))
         elif k == "group":
             cfg.start, cfg.stride = (int(x) for x in v.split(":"))
-        elif k in ("dtype", "values", "path"):
+        elif k in ("dtype", "values", "path", "kind"):
             setattr(cfg, k, v)
         else:
             setattr(cfg, k, int(v))
@@ -115,8 +118,12 @@ def parse_cfg(text: str, base):
 
 
 def gather_bytes(c: GatherCfg) -> float:
-    """Algorithmic bytes: every rank's block read once, W copies of W blocks written."""
+    """Algorithmic bytes: all-gather (and its partitioned form): every rank's
+    block read once, W copies of W blocks written; all-to-all: each of the
+    W x W blocks read once and written once."""
     blk = c.M * c.N * c.es
+    if c.kind == "all_to_all":
+        return 2.0 * c.W * c.W * blk
     return c.W * blk + c.W * c.W * blk
 
 
@@ -374,7 +381,8 @@ def setup_device(dev, g: GatherCfg | None, f: FusedCfg | None, device_inputs: bo
     align = 1 << 16
     sizes = []
     if g:
-        sizes += [("g_in", g.M * g.N * g.es), ("g_out", g.W * g.M * g.N * g.es)]
+        in_rows = g.W * g.M if g.kind == "all_to_all" else g.M
+        sizes += [("g_in", in_rows * g.N * g.es), ("g_out", g.W * g.M * g.N * g.es)]
     if f:
         sizes += [("f_a", f.M * f.K * 2), ("f_out", f.W * f.M * f.N * 2)]
     offs, o = {}, 0
@@ -388,11 +396,12 @@ def setup_device(dev, g: GatherCfg | None, f: FusedCfg | None, device_inputs: bo
     if g:
         dt = gg_inputs.DTYPES[g.dtype]
         draw = gg_inputs.uniform_pm1 if g.values == "uniform" else gg_inputs.normal
+        in_rows = g.W * g.M if g.kind == "all_to_all" else g.M
         for h in g.members():
-            x = draw((g.M, g.N), dt, gen)
+            x = draw((in_rows, g.N), dt, gen)
             if host is not None:
                 host["g_in"][h] = x
-            sh.view(h, offs["g_in"], g.M, g.N, g.N, dt).copy_(x)
+            sh.view(h, offs["g_in"], in_rows, g.N, g.N, dt).copy_(x)
     Bd = None
     if f:
         dt = gg_inputs.DTYPES[f.dtype]
@@ -429,6 +438,15 @@ def sweep_points(name: str):
             for N in (4096, 8192):
                 pts.append((GatherCfg(W=4, M=M, N=N, dtype="f16", start=1, stride=2,
                                       values="normal"), None))
+    elif name == "variants":  # partitioned all-gather, destination grouping, all-to-all
+        for p in (8, 16, 32, 64, 148):
+            pts.append((replace(GATHER, programs=p, kind="partitioned", path="tma"), None))
+        for path in ("tma", "bulk"):
+            for p in (64, 148):
+                for gsz in (1, 2, 4):
+                    pts.append((replace(GATHER, programs=p, dests_per_wait=gsz, path=path), None))
+        for p in (16, 64, 128, 148):
+            pts.append((replace(GATHER, programs=p, kind="all_to_all", path="auto"), None))
     elif name == "fused":  # 8 ranks, M_local 1024/4096/16384, f16 and bf16, + subgroup (0,2,4)
         for path in ("2sm", "1sm"):
             for M in (1024, 4096, 16384):
@@ -441,6 +459,20 @@ def sweep_points(name: str):
     else:
         raise SystemExit(f"unknown sweep {name}")
     return pts
+
+
+def launch_gather(gg, g: GatherCfg, sh, offs, status, dt, stream):
+    """One launch of the configured gather-family collective."""
+    args = (sh.heap, -1, sh.ptr(g.start, offs["g_in"]), g.N, sh.ptr(g.start, offs["g_out"]), g.N,
+            g.M, g.N, dt, (g.bm, g.bn), g.programs, (g.start, g.stride, g.W))
+    if g.kind == "all_to_all":
+        gg.all_to_all(*args, status=status, stream=stream, path=g.path)
+    elif g.kind == "partitioned":
+        gg.all_gather_partitioned(*args, status=status, stream=stream, path=g.path)
+    elif g.dests_per_wait:
+        gg.all_gather_grouped(*args, g.dests_per_wait, status=status, stream=stream, path=g.path)
+    else:
+        gg.all_gather(*args, status=status, stream=stream, path=g.path)
 
 
 def run_sweep(args):
@@ -464,10 +496,7 @@ def run_sweep(args):
 
         def launch():
             if g:
-                gg.all_gather(sh.heap, -1, sh.ptr(g.start, offs["g_in"]), g.N,
-                              sh.ptr(g.start, offs["g_out"]), g.N, g.M, g.N,
-                              gg_inputs.DTYPES[g.dtype], (g.bm, g.bn), g.programs,
-                              (g.start, g.stride, g.W), status=status, path=g.path)
+                launch_gather(gg, g, sh, offs, status, gg_inputs.DTYPES[g.dtype], None)
             else:
                 gg.matmul_all_gather(sh.heap, -1, sh.ptr(f.start, offs["f_a"]), f.K, Bd, f.N,
                                      sh.ptr(f.start, offs["f_out"]), f.N, f.M, f.N, f.K,
@@ -527,7 +556,7 @@ def main():
     ap.add_argument("--device-inputs", default="auto", choices=["auto", "yes", "no"],
                     help="draw inputs on the GPU (seeded) instead of the CPU")
     ap.add_argument("--clocks-out", default=None)
-    ap.add_argument("--sweep", default=None, choices=["budget", "gather", "fused"],
+    ap.add_argument("--sweep", default=None, choices=["budget", "gather", "fused", "variants"],
                     help="time every point of a configuration sweep (one JSON line each)")
     ap.add_argument("--sweep-clocks", action="store_true",
                     help="sample SM clocks while each sweep point runs (about 1 s per point)")
@@ -564,16 +593,14 @@ def main():
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
     gdt = gg_inputs.DTYPES[g.dtype] if g else None
+    g_in_rows = (g.W * g.M if g.kind == "all_to_all" else g.M) if g else 0
     fdt = gg_inputs.DTYPES[f.dtype] if f else None
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
         if g:
-            gg.all_gather(sh.heap, -1, sh.ptr(g.start, offs["g_in"]), g.N,
-                          sh.ptr(g.start, offs["g_out"]), g.N, g.M, g.N, gdt, (g.bm, g.bn),
-                          g.programs, (g.start, g.stride, g.W), status=status, stream=stream,
-                          path=g.path)
+            launch_gather(gg, g, sh, offs, status, gdt, stream)
         if ev is not None:
             ev[1].record(stream)
         if f:
@@ -623,7 +650,7 @@ def main():
             host = {"g_in": {}, "f_a": {}}
             if g:
                 for h in g.members():
-                    host["g_in"][h] = sh.view(h, offs["g_in"], g.M, g.N, g.N, gdt).cpu()
+                    host["g_in"][h] = sh.view(h, offs["g_in"], g_in_rows, g.N, g.N, gdt).cpu()
             if f:
                 for h in f.members():
                     host["f_a"][h] = sh.view(h, offs["f_a"], f.M, f.K, f.K, fdt).cpu()
@@ -641,8 +668,8 @@ def main():
         def e2e_step():
             if g:
                 for h in g.members():
-                    sh.view(h, offs["g_in"], g.M, g.N, g.N, gdt).copy_(pin["g_in"][h],
-                                                                        non_blocking=True)
+                    sh.view(h, offs["g_in"], g_in_rows, g.N, g.N, gdt).copy_(pin["g_in"][h],
+                                                                              non_blocking=True)
             if f:
                 for h in f.members():
                     sh.view(h, offs["f_a"], f.M, f.K, f.K, fdt).copy_(pin["f_a"][h],

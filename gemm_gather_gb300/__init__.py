@@ -14,14 +14,16 @@ from dataclasses import dataclass
 import torch
 
 from ._lib import (GG_AG_AUTO, GG_AG_BULK, GG_AG_TMA, GG_AG_VECTOR, GG_BF16, GG_MAG_1SM, GG_MAG_2SM,
-                   GG_MAG_AUTO, GG_ERR_ALIGNMENT,
+                   GG_MAG_AUTO, GG_COLL_ALL_GATHER, GG_COLL_ALL_GATHER_PARTITIONED,
+                   GG_COLL_ALL_TO_ALL, GG_ERR_ALIGNMENT,
                    GG_ERR_CUDA, GG_ERR_INVALID_ARG, GG_ERR_NOT_IN_HEAP, GG_ERR_TIMEOUT,
                    GG_ERR_UNSUPPORTED, GG_F16, GG_F32, GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N,
                    GG_MAX_WORLD, GG_OK, GGError, Group, Tile, check, lib, LIB_PATH)
 
 __all__ = [
     "heap_create", "heap_wrap", "heap_bases", "heap_info", "heap_destroy", "all_gather",
-    "all_gather_check", "matmul_all_gather", "matmul_all_gather_check", "set_wait_limit_ns",
+    "all_gather_check", "all_gather_grouped", "all_gather_partitioned", "all_to_all",
+    "collective_check", "matmul_all_gather", "matmul_all_gather_check", "set_wait_limit_ns",
     "get_wait_limit_ns", "debug_inject_stall", "SymmetricHeap", "Heap", "GGError", "DTYPE_CODES", "PATHS",
     "FUSED_TILE", "FUSED_PATHS",
 ]
@@ -122,6 +124,52 @@ def all_gather_check(heap: Heap, rank: int, input, ld_in: int, output, ld_out: i
     check(lib.gg_all_gather_check(heap.handle, rank, _ptr(input), ld_in, _ptr(output), ld_out, M,
                                   N, _dtype(dtype), Tile(*tile), comm_programs, Group(*group),
                                   PATHS[path], ctypes.byref(chosen)))
+    return {GG_AG_AUTO: "none", GG_AG_BULK: "bulk", GG_AG_VECTOR: "vector",
+            GG_AG_TMA: "tma"}[chosen.value]
+
+
+def all_gather_grouped(heap: Heap, rank: int, input, ld_in: int, output, ld_out: int, M: int,
+                       N: int, dtype, tile: tuple[int, int], comm_programs: int,
+                       group: tuple[int, int, int], dests_per_wait: int, status=None, stream=None,
+                       path: str = "auto") -> None:
+    check(lib.gg_all_gather_grouped(heap.handle, rank, _ptr(input), ld_in, _ptr(output), ld_out,
+                                    M, N, _dtype(dtype), Tile(*tile), comm_programs, Group(*group),
+                                    dests_per_wait, _ptr(status), _stream(stream), PATHS[path]))
+
+
+def all_gather_partitioned(heap: Heap, rank: int, input, ld_in: int, output, ld_out: int, M: int,
+                           N: int, dtype, tile: tuple[int, int], comm_programs: int,
+                           group: tuple[int, int, int], status=None, stream=None,
+                           path: str = "auto") -> None:
+    check(lib.gg_all_gather_partitioned(heap.handle, rank, _ptr(input), ld_in, _ptr(output),
+                                        ld_out, M, N, _dtype(dtype), Tile(*tile), comm_programs,
+                                        Group(*group), _ptr(status), _stream(stream),
+                                        PATHS[path]))
+
+
+def all_to_all(heap: Heap, rank: int, input, ld_in: int, output, ld_out: int, M: int, N: int,
+               dtype, tile: tuple[int, int], comm_programs: int, group: tuple[int, int, int],
+               status=None, stream=None, path: str = "auto") -> None:
+    check(lib.gg_all_to_all(heap.handle, rank, _ptr(input), ld_in, _ptr(output), ld_out, M, N,
+                            _dtype(dtype), Tile(*tile), comm_programs, Group(*group),
+                            _ptr(status), _stream(stream), PATHS[path]))
+
+
+COLLECTIVES = {"all_gather": GG_COLL_ALL_GATHER,
+               "all_gather_partitioned": GG_COLL_ALL_GATHER_PARTITIONED,
+               "all_to_all": GG_COLL_ALL_TO_ALL}
+
+
+def collective_check(kind: str, heap: Heap, rank: int, input, ld_in: int, output, ld_out: int,
+                     M: int, N: int, dtype, tile: tuple[int, int], comm_programs: int,
+                     group: tuple[int, int, int], dests_per_wait: int = 0,
+                     path: str = "auto") -> str:
+    """Validate without launching; returns the path a launch would take."""
+    chosen = ctypes.c_int()
+    check(lib.gg_collective_check(COLLECTIVES[kind], heap.handle, rank, _ptr(input), ld_in,
+                                  _ptr(output), ld_out, M, N, _dtype(dtype), Tile(*tile),
+                                  comm_programs, Group(*group), dests_per_wait, PATHS[path],
+                                  ctypes.byref(chosen)))
     return {GG_AG_AUTO: "none", GG_AG_BULK: "bulk", GG_AG_VECTOR: "vector",
             GG_AG_TMA: "tma"}[chosen.value]
 

@@ -22,6 +22,7 @@ GG_ERR_TIMEOUT = -6
 GG_F16, GG_BF16, GG_F32 = 0, 1, 2
 GG_AG_AUTO, GG_AG_BULK, GG_AG_VECTOR, GG_AG_TMA = 0, 1, 2, 3
 GG_MAG_AUTO, GG_MAG_1SM, GG_MAG_2SM = 0, 1, 2
+GG_COLL_ALL_GATHER, GG_COLL_ALL_GATHER_PARTITIONED, GG_COLL_ALL_TO_ALL = 0, 1, 2
 GG_MAX_WORLD = 64
 GG_MAX_HEAPS = 1024
 GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N = 128, 256
@@ -29,7 +30,8 @@ GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N = 128, 256
 # Every entry point declared in include/gemm_gather.h.
 EXPORTS = (
     "gg_heap_create", "gg_heap_wrap", "gg_heap_bases", "gg_heap_info", "gg_heap_destroy",
-    "gg_all_gather", "gg_all_gather_path", "gg_all_gather_check",
+    "gg_all_gather", "gg_all_gather_path", "gg_all_gather_check", "gg_all_gather_grouped",
+    "gg_all_gather_partitioned", "gg_all_to_all", "gg_collective_check",
     "gg_matmul_all_gather", "gg_matmul_all_gather_path", "gg_matmul_all_gather_check",
     "gg_set_wait_limit_ns", "gg_get_wait_limit_ns", "gg_debug_inject_stall",
     "gg_last_error", "gg_status_string", "gg_version",
@@ -61,6 +63,14 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
                                 vp, i32], i32),
         "gg_all_gather_check": ([vp, i32, vp, i64, vp, i64, i64, i64, i32, Tile, i32, Group, i32,
                                  ctypes.POINTER(i32)], i32),
+        "gg_all_gather_grouped": ([vp, i32, vp, i64, vp, i64, i64, i64, i32, Tile, i32, Group,
+                                   i32, vp, vp, i32], i32),
+        "gg_all_gather_partitioned": ([vp, i32, vp, i64, vp, i64, i64, i64, i32, Tile, i32, Group,
+                                       vp, vp, i32], i32),
+        "gg_all_to_all": ([vp, i32, vp, i64, vp, i64, i64, i64, i32, Tile, i32, Group, vp, vp, i32],
+                          i32),
+        "gg_collective_check": ([i32, vp, i32, vp, i64, vp, i64, i64, i64, i32, Tile, i32, Group,
+                                 i32, i32, ctypes.POINTER(i32)], i32),
         "gg_matmul_all_gather": ([vp, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, i32, Tile,
                                   i32, Group, vp, vp], i32),
         "gg_matmul_all_gather_path": ([vp, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, i32,

@@ -29,6 +29,19 @@
 //            that read it have finished reading shared memory.
 //  * vector: 16/8/4/2-byte loads into registers, then one store per
 //            destination; several tiles' loads are in flight per thread.
+//
+// The same kernels run the two neighbouring collectives of the pages:
+//  * partitioned all-gather (iris PR #626, "Triton CCL all-gather":
+//    persistent_all_gather_partitioned): programs are split across the
+//    destinations; program p serves destination p mod W only, so each tile is
+//    read once per destination (tensor-map and vector paths);
+//  * all-to-all (iris #594 "Compiler inspection and grouping", iris #591
+//    Work): member i's input holds W row blocks; block d goes to row block i
+//    of member d's output, one store per tile (tensor-map and vector paths).
+// and the destination grouping of iris #594 "Compiler inspection and
+// grouping" / iris #591 Description §2: with dests_per_wait = G the stores of
+// a tile go out G destinations at a time, each group waiting until the
+// previous ones have read shared memory (bulk and tensor-map paths).
 #include <cuda_runtime.h>
 
 #include "gg_internal.h"
@@ -56,17 +69,54 @@ constexpr int kAgHeader = (int)((sizeof(AgShared) + 127) / 128 * 128);
 
 struct Item {
     int g;          // group index of the source
+    int d;          // group index of the destination block (all-to-all), else -1
     int64_t tm, tn; // tile coordinates
     int rows;       // valid rows of the tile
     uint32_t rb;    // valid bytes per tile row
 };
 
+// The items one pipeline (warp) of a program walks: first, first + step, ...
+// and, for the partitioned all-gather, the one destination its program serves.
+struct Walk {
+    int64_t first, step, n;
+    int dest;
+};
+
+__device__ __forceinline__ Walk make_walk(const GatherArgs &a, int warp, int npipe)
+{
+    int64_t prog = blockIdx.x, nprog = gridDim.x;
+    int dest = -1;
+    if (a.mode == kModePartitioned) {  // program p serves destination p mod W
+        dest = (int)(blockIdx.x % (unsigned)a.W);
+        prog = blockIdx.x / (unsigned)a.W;
+        nprog = (gridDim.x - 1 - dest) / a.W + 1;
+    }
+    Walk w;
+    w.first = prog + (int64_t)warp * nprog;
+    w.step = nprog * npipe;
+    w.n = w.first < a.total_items ? (a.total_items - 1 - w.first) / w.step + 1 : 0;
+    w.dest = dest;
+    return w;
+}
+
+// Item t: source-major; for the all-to-all each source's items run over its W
+// destination blocks in rotated order (its own block first), then tiles.
 __device__ __forceinline__ Item decode_item(const GatherArgs &a, int64_t t)
 {
     Item it;
-    const int64_t s = t / a.tiles_per_src;
-    const int64_t tile = t - s * a.tiles_per_src;
+    const int64_t per_src = a.mode == kModeAllToAll ? a.tiles_per_src * a.W : a.tiles_per_src;
+    const int64_t s = t / per_src;
+    int64_t tile = t - s * per_src;
     it.g = a.src_first + (int)s;
+    it.d = -1;
+    if (a.mode == kModeAllToAll) {
+        const int jr = (int)(tile / a.tiles_per_src);
+        tile -= (int64_t)jr * a.tiles_per_src;
+        int d = it.g + jr;
+        if (d >= a.W)
+            d -= a.W;
+        it.d = d;
+    }
     it.tm = tile / a.tiles_n;
     it.tn = tile - it.tm * a.tiles_n;
     const int64_t r0 = it.tm * a.bm;
@@ -88,6 +138,16 @@ __device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap *ma
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
         "[%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_box4(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                              int c2, int c3, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], "
+        "[%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
         : "memory");
 }
 
@@ -142,6 +202,7 @@ __global__ void __launch_bounds__(kAgWarps * 32)
     const uint32_t ring = ptx::smem_addr(smem + kAgHeader) + (uint32_t)(warp * stages * stage_bytes);
     const uint32_t full0 = ptx::smem_addr(&sh.full[warp][0]);
     const uint32_t pitch = (uint32_t)a.bn_b;  // staged row pitch (multiple of 16)
+    const int grp = (a.dests_per_wait > 0 && a.dests_per_wait < a.W) ? a.dests_per_wait : a.W;
 
     auto issue_load = [&](int64_t k) {
         const Item it = decode_item(a, first + k * step);
@@ -177,18 +238,27 @@ __global__ void __launch_bounds__(kAgWarps * 32)
         const uint32_t buf = ring + (uint32_t)st * stage_bytes;
         const int64_t row0 = (int64_t)it.g * a.M + it.tm * a.bm;
         const int64_t col0 = it.tn * a.bn_b;
-        const int pairs = it.rows * a.W;
-        // pair p -> destination j = p / rows (j = 0 is the local copy), row p % rows
-        for (int p = lane; p < pairs; p += 32) {
-            const int j = p / it.rows;
-            const int r = p - j * it.rows;
-            int i = it.g + j;
-            if (i >= a.W)
-                i -= a.W;
-            uint8_t *dst = reinterpret_cast<uint8_t *>(sh.dst[i]) + (row0 + r) * a.ld_out_b + col0;
-            ptx::bulk_s2g(dst, buf + (uint32_t)r * pitch, it.rb);
+        // destinations go out `grp` at a time (all at once unless grouped);
+        // pair p of a group -> destination j0 + p / rows (j = 0 is the local
+        // copy), row p % rows
+        for (int j0 = 0; j0 < a.W; j0 += grp) {
+            const int nj = a.W - j0 < grp ? a.W - j0 : grp;
+            for (int p = lane; p < nj * it.rows; p += 32) {
+                const int jj = p / it.rows;
+                const int r = p - jj * it.rows;
+                int i = it.g + j0 + jj;
+                if (i >= a.W)
+                    i -= a.W;
+                uint8_t *dst =
+                    reinterpret_cast<uint8_t *>(sh.dst[i]) + (row0 + r) * a.ld_out_b + col0;
+                ptx::bulk_s2g(dst, buf + (uint32_t)r * pitch, it.rb);
+            }
+            ptx::bulk_commit();
+            if (j0 + grp < a.W) {  // the next group waits until this one has read its data
+                ptx::bulk_wait_read<0>();
+                __syncwarp();
+            }
         }
-        ptx::bulk_commit();
         const int64_t kk = k + lookahead;
         if (kk < n_local) {
             if (kk >= stages) {
@@ -213,6 +283,7 @@ __global__ void __launch_bounds__(kAgWarps * 32)
 }
 
 // Tensor-map path: same ring pipeline as ag_bulk_kernel; a tile is one box.
+// in_map views the sources as {N, M, heaps} (all-to-all: {N, M, W, heaps}).
 template <int D>
 __global__ void __launch_bounds__(kAgWarps * 32)
     ag_tma_kernel(const __grid_constant__ CUtensorMap in_map, const __grid_constant__ OutMaps out,
@@ -235,14 +306,14 @@ __global__ void __launch_bounds__(kAgWarps * 32)
         tma_prefetch(&out.map[threadIdx.x]);
     __syncthreads();
 
-    const int64_t step = (int64_t)gridDim.x * npipe;
-    const int64_t first = blockIdx.x + (int64_t)warp * gridDim.x;
-    const int64_t n_local = first < a.total_items ? (a.total_items - 1 - first) / step + 1 : 0;
+    const Walk walk = make_walk(a, warp, npipe);
+    const int64_t first = walk.first, step = walk.step, n_local = walk.n;
     const int lookahead = stages - D;
     const uint32_t ring = ptx::smem_addr(smem + kAgHeader) + (uint32_t)(warp * stages * stage_bytes);
     const uint32_t full0 = ptx::smem_addr(&sh.full[warp][0]);
     const uint32_t box_bytes = (uint32_t)(a.bm * a.bn_b);  // a full box, clipped parts zero-filled
     const int bn = (int)(a.bn_b / a.es);
+    const int grp = (a.dests_per_wait > 0 && a.dests_per_wait < a.W) ? a.dests_per_wait : a.W;
 
     auto issue_load = [&](int64_t k) {
         const Item it = decode_item(a, first + k * step);
@@ -253,8 +324,11 @@ __global__ void __launch_bounds__(kAgWarps * 32)
         if (lane == 0) {
             ptx::mbar_arrive_expect_tx(bar, box_bytes);
             const int h = a.in_abs ? 0 : a.rank_start + it.g * a.rank_stride;
-            tma_load_box(ring + (uint32_t)st * stage_bytes, &in_map, (int)it.tn * bn,
-                         (int)(it.tm * a.bm), h, bar);
+            const uint32_t dst = ring + (uint32_t)st * stage_bytes;
+            if (a.mode == kModeAllToAll)
+                tma_load_box4(dst, &in_map, (int)it.tn * bn, (int)(it.tm * a.bm), it.d, h, bar);
+            else
+                tma_load_box(dst, &in_map, (int)it.tn * bn, (int)(it.tm * a.bm), h, bar);
         }
         __syncwarp();
     };
@@ -275,14 +349,31 @@ __global__ void __launch_bounds__(kAgWarps * 32)
         }
         const Item it = decode_item(a, first + k * step);
         const uint32_t buf = ring + (uint32_t)st * stage_bytes;
-        // lane j stores the tile to destination j: the local copy first, peers rotated
-        for (int j = lane; j < a.W; j += 32) {
-            int i = it.g + j;
-            if (i >= a.W)
-                i -= a.W;
-            tma_store_box(&out.map[i], buf, (int)it.tn * bn, (int)(it.tm * a.bm), it.g);
+        const int c0 = (int)it.tn * bn, c1 = (int)(it.tm * a.bm);
+        if (a.mode == kModeGather) {
+            // lane j stores to destination j of the group: the local copy first,
+            // peers rotated; `grp` destinations per wait
+            for (int j0 = 0; j0 < a.W; j0 += grp) {
+                const int jend = j0 + grp < a.W ? j0 + grp : a.W;
+                for (int j = j0 + lane; j < jend; j += 32) {
+                    int i = it.g + j;
+                    if (i >= a.W)
+                        i -= a.W;
+                    tma_store_box(&out.map[i], buf, c0, c1, it.g);
+                }
+                ptx::bulk_commit();
+                if (jend < a.W) {
+                    ptx::bulk_wait_read<0>();
+                    __syncwarp();
+                }
+            }
+        } else {
+            // one destination: the program's own (partitioned) or the block's (all-to-all)
+            if (lane == 0)
+                tma_store_box(&out.map[a.mode == kModePartitioned ? walk.dest : it.d], buf, c0, c1,
+                              it.g);
+            ptx::bulk_commit();
         }
-        ptx::bulk_commit();
         const int64_t kk = k + lookahead;
         if (kk < n_local) {
             if (kk >= stages) {
@@ -329,9 +420,10 @@ __global__ void __launch_bounds__(kVecThreads) ag_vec_kernel(const GatherArgs a)
 
     const int crow = (int)(a.bn_b / VB);           // vectors per full tile row
     const int tile_vecs = a.bm * crow;             // vectors per full tile
-    const int64_t stride = (int64_t)gridDim.x * kVecUnroll;
+    const Walk walk = make_walk(a, 0, 1);          // the whole program walks one item list
+    const int64_t stride = walk.step * kVecUnroll;
 
-    for (int64_t base = blockIdx.x; base < a.total_items; base += stride) {
+    for (int64_t base = walk.first; base < a.total_items; base += stride) {
         for (int c = threadIdx.x; c < tile_vecs; c += blockDim.x) {
             const int r = c / crow;
             const int cc = c - r * crow;
@@ -340,15 +432,17 @@ __global__ void __launch_bounds__(kVecThreads) ag_vec_kernel(const GatherArgs a)
             Item it[kVecUnroll];
 #pragma unroll
             for (int u = 0; u < kVecUnroll; ++u) {
-                const int64_t t = base + (int64_t)u * gridDim.x;
+                const int64_t t = base + (int64_t)u * walk.step;
                 valid[u] = false;
                 if (t < a.total_items) {
                     it[u] = decode_item(a, t);
                     valid[u] = r < it[u].rows && (uint32_t)cc * VB < it[u].rb;
                     if (valid[u]) {
+                        // all-to-all: the source's block d starts at row d*M
+                        const int64_t srow = (it[u].d >= 0 ? (int64_t)it[u].d * a.M : 0) +
+                                             it[u].tm * a.bm + r;
                         const uint8_t *s = reinterpret_cast<const uint8_t *>(src[it[u].g]) +
-                                           (it[u].tm * a.bm + r) * a.ld_in_b + it[u].tn * a.bn_b +
-                                           (int64_t)cc * VB;
+                                           srow * a.ld_in_b + it[u].tn * a.bn_b + (int64_t)cc * VB;
                         v[u] = *reinterpret_cast<const V *>(s);
                     }
                 }
@@ -359,10 +453,15 @@ __global__ void __launch_bounds__(kVecThreads) ag_vec_kernel(const GatherArgs a)
                     continue;
                 const int64_t off = ((int64_t)it[u].g * a.M + it[u].tm * a.bm + r) * a.ld_out_b +
                                     it[u].tn * a.bn_b + (int64_t)cc * VB;
-                for (int j = 0; j < a.W; ++j) {
-                    int i = it[u].g + j;
-                    if (i >= a.W)
-                        i -= a.W;
+                if (a.mode == kModeGather) {
+                    for (int j = 0; j < a.W; ++j) {
+                        int i = it[u].g + j;
+                        if (i >= a.W)
+                            i -= a.W;
+                        *reinterpret_cast<V *>(reinterpret_cast<uint8_t *>(dst[i]) + off) = v[u];
+                    }
+                } else {
+                    const int i = a.mode == kModePartitioned ? walk.dest : it[u].d;
                     *reinterpret_cast<V *>(reinterpret_cast<uint8_t *>(dst[i]) + off) = v[u];
                 }
             }

@@ -207,11 +207,12 @@ namespace {
 // Data path a gather launch takes.
 enum GatherKind { kVector = 0, kBulk = 1, kTma = 2 };
 
-gg_status prepare_gather(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
-                         void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
-                         gg_tile tile, int comm_programs, gg_group group, int *dev_status,
-                         gg_ag_path path, gg::GatherArgs *out_args, int *kind, int *vec_bytes,
-                         CUtensorMap *in_map, gg::OutMaps *maps, bool *launch)
+gg_status prepare_gather(const gg_heap *heap, int mode, int rank, const void *input,
+                         int64_t ld_in, void *output, int64_t ld_out, int64_t M, int64_t N,
+                         gg_dtype dtype, gg_tile tile, int comm_programs, gg_group group,
+                         int dests_per_wait, int *dev_status, gg_ag_path path,
+                         gg::GatherArgs *out_args, int *kind, int *vec_bytes, CUtensorMap *in_map,
+                         gg::OutMaps *maps, bool *launch)
 {
     *launch = false;
     int gi = -1;
@@ -239,15 +240,28 @@ gg_status prepare_gather(const gg_heap *heap, int rank, const void *input, int64
                     tile.block_m, tile.block_n, es);
     if (comm_programs < 1 || comm_programs > 65535)
         return fail(GG_ERR_INVALID_ARG, "comm_programs %d outside [1, 65535]", comm_programs);
+    if (dests_per_wait < 0)
+        return fail(GG_ERR_INVALID_ARG, "dests_per_wait %d must be >= 0", dests_per_wait);
+    if (mode == gg::kModePartitioned && comm_programs < group.world_size)
+        return fail(GG_ERR_INVALID_ARG,
+                    "the partitioned all-gather needs comm_programs (%d) >= world_size (%d): one "
+                    "destination per program",
+                    comm_programs, group.world_size);
+    if (mode != gg::kModeGather && path == GG_AG_BULK)
+        return fail(GG_ERR_UNSUPPORTED,
+                    "the partitioned all-gather and the all-to-all run the tensor-map or the "
+                    "vector path");
     if (!output || (!input && M > 0 && N > 0))
         return fail(GG_ERR_INVALID_ARG, "input and output must be non-NULL");
     if (M == 0 || N == 0)
         return ok();
 
     const int W = group.world_size;
+    // the all-to-all input holds W row blocks (one per destination)
+    const int64_t in_rows = mode == gg::kModeAllToAll ? (int64_t)W * M : M;
     int64_t rows_out, out_ext, in_ext, tmp;
     if (!checked_mul(W, M, &rows_out) || !checked_mul(rows_out - 1, ld_out, &tmp) ||
-        !checked_mul(tmp + N, es, &out_ext) || !checked_mul(M - 1, ld_in, &tmp) ||
+        !checked_mul(tmp + N, es, &out_ext) || !checked_mul(in_rows - 1, ld_in, &tmp) ||
         !checked_mul(tmp + N, es, &in_ext))
         return fail(GG_ERR_INVALID_ARG, "sizes overflow");
     int64_t out_off = 0;
@@ -295,8 +309,10 @@ gg_status prepare_gather(const gg_heap *heap, int rank, const void *input, int64
     a.bn_b = (int64_t)tile.block_n * es;
     a.tiles_n = ceil_div(N, tile.block_n);
     a.tiles_per_src = ceil_div(M, tile.block_m) * a.tiles_n;
-    a.total_items = a.tiles_per_src * a.n_src;
+    a.total_items = a.tiles_per_src * a.n_src * (mode == gg::kModeAllToAll ? W : 1);
     a.es = es;
+    a.mode = mode;
+    a.dests_per_wait = dests_per_wait;
     a.status = dev_status;
     a.wait_limit_ns = g_wait_limit_ns.load();
     a.inject_stall = g_inject_stall.load();
@@ -322,7 +338,7 @@ gg_status prepare_gather(const gg_heap *heap, int rank, const void *input, int64
     int k;
     if (path == GG_AG_TMA || (path == GG_AG_AUTO && tma_ok))
         k = kTma;
-    else if (path == GG_AG_BULK || (path == GG_AG_AUTO && bulk_ok))
+    else if (path == GG_AG_BULK || (path == GG_AG_AUTO && bulk_ok && mode == gg::kModeGather))
         k = kBulk;
     else
         k = kVector;
@@ -331,16 +347,29 @@ gg_status prepare_gather(const gg_heap *heap, int rank, const void *input, int64
     if (k == kTma && in_map && maps) {
         const CUtensorMapDataType dt =
             es == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
-        const uint32_t box[3] = {(uint32_t)tile.block_n, (uint32_t)tile.block_m, 1};
-        const uint64_t dims[3] = {(uint64_t)N, (uint64_t)M,
-                                  (uint64_t)(rank == -1 ? heap->H : 1)};
-        const uint64_t strides[2] = {(uint64_t)a.ld_in_b,
-                                     rank == -1 ? (uint64_t)heap->part
-                                                : (uint64_t)(M * a.ld_in_b)};
         const void *ibase = rank == -1 ? reinterpret_cast<const void *>(heap->base + a.in_off)
                                        : input;
-        if (!gg::encode_map(in_map, dt, 3, ibase, dims, strides, box,
-                            CU_TENSOR_MAP_SWIZZLE_NONE))
+        const uint64_t whole = (uint64_t)(in_rows * a.ld_in_b);  // one source's input
+        bool enc;
+        if (mode == gg::kModeAllToAll) {
+            // sources as {N, M, W blocks, heaps}: a tile clips at the end of its block
+            const uint32_t box[4] = {(uint32_t)tile.block_n, (uint32_t)tile.block_m, 1, 1};
+            const uint64_t dims[4] = {(uint64_t)N, (uint64_t)M, (uint64_t)W,
+                                      (uint64_t)(rank == -1 ? heap->H : 1)};
+            const uint64_t strides[3] = {(uint64_t)a.ld_in_b, (uint64_t)(M * a.ld_in_b),
+                                         rank == -1 ? (uint64_t)heap->part : whole};
+            enc = gg::encode_map(in_map, dt, 4, ibase, dims, strides, box,
+                                 CU_TENSOR_MAP_SWIZZLE_NONE);
+        } else {
+            const uint32_t box[3] = {(uint32_t)tile.block_n, (uint32_t)tile.block_m, 1};
+            const uint64_t dims[3] = {(uint64_t)N, (uint64_t)M,
+                                      (uint64_t)(rank == -1 ? heap->H : 1)};
+            const uint64_t strides[2] = {(uint64_t)a.ld_in_b,
+                                         rank == -1 ? (uint64_t)heap->part : whole};
+            enc = gg::encode_map(in_map, dt, 3, ibase, dims, strides, box,
+                                 CU_TENSOR_MAP_SWIZZLE_NONE);
+        }
+        if (!enc)
             return fail(GG_ERR_CUDA, "encoding the input tensor map");
         uint64_t member_out[GG_MAX_WORLD];
         for (int q = 0; q < W; ++q)
@@ -360,19 +389,20 @@ gg_status prepare_gather(const gg_heap *heap, int rank, const void *input, int64
 
 extern "C" {
 
-gg_status gg_all_gather_path(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
-                             void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
-                             gg_tile tile, int comm_programs, gg_group group, int *dev_status,
-                             gg_stream_t stream, gg_ag_path path)
+// Validate, build and launch one collective of the gather kernels.
+gg_status run_collective(const gg_heap *heap, int mode, int rank, const void *input, int64_t ld_in,
+                         void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
+                         gg_tile tile, int comm_programs, gg_group group, int dests_per_wait,
+                         int *dev_status, gg_stream_t stream, gg_ag_path path)
 {
     gg::GatherArgs a;
     int kind = kVector, vec = 0;
     bool launch = false;
     static thread_local CUtensorMap in_map;
     static thread_local gg::OutMaps maps;
-    gg_status st = prepare_gather(heap, rank, input, ld_in, output, ld_out, M, N, dtype, tile,
-                                  comm_programs, group, dev_status, path, &a, &kind, &vec,
-                                  &in_map, &maps, &launch);
+    gg_status st = prepare_gather(heap, mode, rank, input, ld_in, output, ld_out, M, N, dtype, tile,
+                                  comm_programs, group, dests_per_wait, dev_status, path, &a, &kind,
+                                  &vec, &in_map, &maps, &launch);
     if (st != GG_OK || !launch)
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -384,8 +414,69 @@ gg_status gg_all_gather_path(const gg_heap *heap, int rank, const void *input, i
     else
         e = gg::launch_gather_vec(a, comm_programs, vec, s);
     if (e != cudaSuccess)
-        return cuda_fail(e, "launching the all-gather");
+        return cuda_fail(e, "launching the collective");
     return ok();
+}
+
+gg_status gg_all_gather_path(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
+                             void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
+                             gg_tile tile, int comm_programs, gg_group group, int *dev_status,
+                             gg_stream_t stream, gg_ag_path path)
+{
+    return run_collective(heap, gg::kModeGather, rank, input, ld_in, output, ld_out, M, N, dtype,
+                          tile, comm_programs, group, 0, dev_status, stream, path);
+}
+
+gg_status gg_all_gather_grouped(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
+                                void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
+                                gg_tile tile, int comm_programs, gg_group group,
+                                int dests_per_wait, int *dev_status, gg_stream_t stream,
+                                gg_ag_path path)
+{
+    return run_collective(heap, gg::kModeGather, rank, input, ld_in, output, ld_out, M, N, dtype,
+                          tile, comm_programs, group, dests_per_wait, dev_status, stream, path);
+}
+
+gg_status gg_all_gather_partitioned(const gg_heap *heap, int rank, const void *input,
+                                    int64_t ld_in, void *output, int64_t ld_out, int64_t M,
+                                    int64_t N, gg_dtype dtype, gg_tile tile, int comm_programs,
+                                    gg_group group, int *dev_status, gg_stream_t stream,
+                                    gg_ag_path path)
+{
+    return run_collective(heap, gg::kModePartitioned, rank, input, ld_in, output, ld_out, M, N,
+                          dtype, tile, comm_programs, group, 0, dev_status, stream, path);
+}
+
+gg_status gg_all_to_all(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
+                        void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
+                        gg_tile tile, int comm_programs, gg_group group, int *dev_status,
+                        gg_stream_t stream, gg_ag_path path)
+{
+    return run_collective(heap, gg::kModeAllToAll, rank, input, ld_in, output, ld_out, M, N, dtype,
+                          tile, comm_programs, group, 0, dev_status, stream, path);
+}
+
+gg_status gg_collective_check(gg_collective kind, const gg_heap *heap, int rank, const void *input,
+                              int64_t ld_in, void *output, int64_t ld_out, int64_t M, int64_t N,
+                              gg_dtype dtype, gg_tile tile, int comm_programs, gg_group group,
+                              int dests_per_wait, gg_ag_path path, gg_ag_path *chosen)
+{
+    if (kind != GG_COLL_ALL_GATHER && kind != GG_COLL_ALL_GATHER_PARTITIONED &&
+        kind != GG_COLL_ALL_TO_ALL)
+        return fail(GG_ERR_INVALID_ARG, "unknown collective %d", (int)kind);
+    const int mode = kind == GG_COLL_ALL_GATHER
+                         ? gg::kModeGather
+                         : (kind == GG_COLL_ALL_TO_ALL ? gg::kModeAllToAll : gg::kModePartitioned);
+    gg::GatherArgs a;
+    int k = kVector, vec = 0;
+    bool launch = false;
+    gg_status st = prepare_gather(heap, mode, rank, input, ld_in, output, ld_out, M, N, dtype, tile,
+                                  comm_programs, group, dests_per_wait, nullptr, path, &a, &k, &vec,
+                                  nullptr, nullptr, &launch);
+    if (chosen)
+        *chosen = !launch ? GG_AG_AUTO
+                          : (k == kTma ? GG_AG_TMA : (k == kBulk ? GG_AG_BULK : GG_AG_VECTOR));
+    return st;
 }
 
 gg_status gg_all_gather_check(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
@@ -393,16 +484,8 @@ gg_status gg_all_gather_check(const gg_heap *heap, int rank, const void *input, 
                               gg_tile tile, int comm_programs, gg_group group, gg_ag_path path,
                               gg_ag_path *chosen)
 {
-    gg::GatherArgs a;
-    int kind = kVector, vec = 0;
-    bool launch = false;
-    gg_status st = prepare_gather(heap, rank, input, ld_in, output, ld_out, M, N, dtype, tile,
-                                  comm_programs, group, nullptr, path, &a, &kind, &vec, nullptr,
-                                  nullptr, &launch);
-    if (chosen)
-        *chosen = !launch ? GG_AG_AUTO
-                          : (kind == kTma ? GG_AG_TMA : (kind == kBulk ? GG_AG_BULK : GG_AG_VECTOR));
-    return st;
+    return gg_collective_check(GG_COLL_ALL_GATHER, heap, rank, input, ld_in, output, ld_out, M, N,
+                               dtype, tile, comm_programs, group, 0, path, chosen);
 }
 
 gg_status gg_all_gather(const gg_heap *heap, int rank, const void *input, int64_t ld_in,

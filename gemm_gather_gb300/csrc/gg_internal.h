@@ -10,6 +10,11 @@ namespace gg {
 constexpr int kMaxWorld = 64;
 constexpr int kStatusTimeout = -6;  // GG_ERR_TIMEOUT
 
+// Collectives the gather kernels run.
+constexpr int kModeGather = 0;       // every tile to every member
+constexpr int kModePartitioned = 1;  // program p serves member p mod W only
+constexpr int kModeAllToAll = 2;     // member i's block d to member d's block i
+
 // One TMA tensor map per group member's gathered output (kernel parameter).
 struct OutMaps {
     CUtensorMap map[kMaxWorld];
@@ -27,10 +32,11 @@ bool encode_out_maps(OutMaps *out, const uint64_t *member_out, int W, int64_t M,
                      int64_t ld_out_b, int es, uint32_t box_cols, uint32_t box_rows,
                      CUtensorMapDataType dt, CUtensorMapSwizzle swizzle);
 
-// One launch of the tiled all-gather.  A "source" is a group member whose
-// M x N block is gathered; a launch covers n_src consecutive group indices
-// starting at src_first.  Work item t (0 <= t < n_src * tiles_per_src) is
-// tile (t mod tiles_per_src) of source src_first + t / tiles_per_src.
+// One launch of the tiled all-gather (or of its partitioned form, or of the
+// all-to-all).  A "source" is a group member whose M x N block is gathered; a
+// launch covers n_src consecutive group indices starting at src_first.  Work
+// item t (0 <= t < n_src * tiles_per_src, times W for the all-to-all) is a
+// tile of source src_first + t / (items per source).
 struct GatherArgs {
     const uint64_t *bases;  // device heap-bases table, one entry per heap
     int W, rank_start, rank_stride;
@@ -45,6 +51,8 @@ struct GatherArgs {
     int64_t bn_b;               // tile row bytes (block_n * element size)
     int64_t tiles_n, tiles_per_src, total_items;
     int es;                     // element size (bytes)
+    int mode;                   // kModeGather / kModePartitioned / kModeAllToAll
+    int dests_per_wait;         // destinations stored per wait (0: all at once)
     int *status;
     uint64_t wait_limit_ns;
     int inject_stall;  // test hook: program 0 never arms its first stage

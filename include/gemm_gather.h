@@ -171,6 +171,70 @@ gg_status gg_all_gather_check(const gg_heap *heap, int rank, const void *input, 
                               gg_ag_path *chosen);
 
 /* ---------------------------------------------------------------------------
+ * gg_all_gather_grouped — gg_all_gather_path whose tile stores go out
+ * `dests_per_wait` destinations at a time: each group of stores waits until
+ * the previous group has finished reading shared memory (the "INLINE"
+ * grouping of iris #594, "Compiler inspection and grouping", and iris #591,
+ * Description §2: a bounded number of destination stores per wait).
+ * dests_per_wait = 0 (or >= world_size) stores to all destinations at once,
+ * as gg_all_gather does.  Same result.  Applies to the tensor-map and bulk
+ * paths; the vector path ignores it.
+ * ------------------------------------------------------------------------- */
+gg_status gg_all_gather_grouped(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
+                                void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
+                                gg_tile tile, int comm_programs, gg_group group,
+                                int dests_per_wait, int *dev_status, gg_stream_t stream,
+                                gg_ag_path path);
+
+/* ---------------------------------------------------------------------------
+ * gg_all_gather_partitioned — the same result as gg_all_gather, with the
+ * programs partitioned across the destinations (iris PR #626, "Triton CCL
+ * all-gather": persistent_all_gather_partitioned): program p serves group
+ * member p mod world_size only, and the programs of one destination share
+ * all tiles; every tile is therefore read once per destination.  Requires
+ * comm_programs >= world_size (else GG_ERR_INVALID_ARG).  path: GG_AG_AUTO,
+ * GG_AG_TMA or GG_AG_VECTOR (GG_AG_BULK returns GG_ERR_UNSUPPORTED).
+ * ------------------------------------------------------------------------- */
+gg_status gg_all_gather_partitioned(const gg_heap *heap, int rank, const void *input,
+                                    int64_t ld_in, void *output, int64_t ld_out, int64_t M,
+                                    int64_t N, gg_dtype dtype, gg_tile tile, int comm_programs,
+                                    gg_group group, int *dev_status, gg_stream_t stream,
+                                    gg_ag_path path);
+
+/* ---------------------------------------------------------------------------
+ * gg_all_to_all — the all-to-all over the same heap (iris #594, "Compiler
+ * inspection and grouping", and iris #591, Work: Gluon all_to_all).  Member
+ * i's input is world_size*M x N (row pitch ld_in): row block d
+ * (rows d*M .. d*M+M-1) is meant for member d.  Member d's output
+ * (world_size*M x N, pitch ld_out) receives, in row block i, member i's
+ * block d -- torch.distributed.all_to_all_single with equal splits.  Each
+ * tile is read once and stored once; every source sends to its destinations
+ * in rotated order (its own block first).
+ * rank >= 0: only that member's W blocks go out (input: any device memory);
+ * rank == -1: every member, input symmetric.  Other arguments, alignment and
+ * errors as gg_all_gather; path: GG_AG_AUTO, GG_AG_TMA or GG_AG_VECTOR.
+ * ------------------------------------------------------------------------- */
+gg_status gg_all_to_all(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
+                        void *output, int64_t ld_out, int64_t M, int64_t N, gg_dtype dtype,
+                        gg_tile tile, int comm_programs, gg_group group, int *dev_status,
+                        gg_stream_t stream, gg_ag_path path);
+
+/* Collectives of gg_collective_check. */
+typedef enum {
+    GG_COLL_ALL_GATHER = 0,
+    GG_COLL_ALL_GATHER_PARTITIONED = 1,
+    GG_COLL_ALL_TO_ALL = 2
+} gg_collective;
+
+/* Validate a call of one of the collectives above exactly as the launching
+ * call does and launch nothing; *chosen (nullable) receives the path a launch
+ * would take (GG_AG_AUTO when there is nothing to launch). */
+gg_status gg_collective_check(gg_collective kind, const gg_heap *heap, int rank, const void *input,
+                              int64_t ld_in, void *output, int64_t ld_out, int64_t M, int64_t N,
+                              gg_dtype dtype, gg_tile tile, int comm_programs, gg_group group,
+                              int dests_per_wait, gg_ag_path path, gg_ag_path *chosen);
+
+/* ---------------------------------------------------------------------------
  * gg_matmul_all_gather — the fused form (iris PR #626, "Summary" and
  * "Benchmark": the matmul's epilogue all-gathers each output tile).
  * Member r computes C_r = A_r @ B (A_r: M x K row-major, row pitch lda;

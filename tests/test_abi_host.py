@@ -192,3 +192,39 @@ def test_page_facts_tile_geometry():
     assert p["world_size"] - 1 == p["peer_destinations"]
     r = facts["rotated_order"]
     assert [(r["rank"] + j) % r["world_size"] for j in range(r["world_size"])] == r["order"]
+
+
+def coll(heap, kind, **kw):
+    a = dict(rank=-1, input=BASE + 4096, ld_in=256, output=BASE + (1 << 20), ld_out=256, M=64,
+             N=256, dtype=torch.float16, tile=(8, 256), comm_programs=16, group=(0, 1, 4),
+             dests_per_wait=0, path="auto")
+    a.update(kw)
+    return gg.collective_check(kind, heap, a["rank"], a["input"], a["ld_in"], a["output"],
+                               a["ld_out"], a["M"], a["N"], a["dtype"], a["tile"],
+                               a["comm_programs"], a["group"], a["dests_per_wait"], a["path"])
+
+
+def test_next_collectives_valid(heap):
+    assert coll(heap, "all_gather", dests_per_wait=2) == "tma"
+    assert coll(heap, "all_gather", dests_per_wait=2, path="bulk") == "bulk"
+    assert coll(heap, "all_gather_partitioned") == "tma"
+    assert coll(heap, "all_gather_partitioned", comm_programs=4) == "tma"
+    assert coll(heap, "all_gather_partitioned", path="vector") == "vector"
+    assert coll(heap, "all_to_all") == "tma"
+    assert coll(heap, "all_to_all", input=BASE + 4098) == "vector"
+    assert coll(heap, "all_to_all", rank=2, input=TABLE) == "tma"
+
+
+@pytest.mark.parametrize("kind,kw,status", [
+    ("all_gather", dict(dests_per_wait=-1), _lib.GG_ERR_INVALID_ARG),
+    ("all_gather_partitioned", dict(comm_programs=3), _lib.GG_ERR_INVALID_ARG),  # < W
+    ("all_gather_partitioned", dict(path="bulk"), _lib.GG_ERR_UNSUPPORTED),
+    ("all_to_all", dict(path="bulk"), _lib.GG_ERR_UNSUPPORTED),
+    # the all-to-all input is W*M rows: 4 x 64 rows of 512 B overlap the output at +1 MB
+    ("all_to_all", dict(input=BASE + (1 << 20) - 4 * 64 * 512 + 512), _lib.GG_ERR_INVALID_ARG),
+    ("all_to_all", dict(input=BASE + PART - 64 * 512), _lib.GG_ERR_NOT_IN_HEAP),
+])
+def test_next_collectives_reject(heap, kind, kw, status):
+    with pytest.raises(gg.GGError) as e:
+        coll(heap, kind, **kw)
+    assert e.value.status == status, str(e.value)

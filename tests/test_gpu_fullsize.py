@@ -178,3 +178,48 @@ def test_fused_full_size(oracle, case):
         ref = oracle.matmul_f64(a_rows, Bbits, fmt)
         got = out[torch.from_numpy(i * M + rows).cuda()].to(torch.float64).cpu().numpy()
         check_tolerance(got, ref, dtype)
+
+
+def test_all_to_all_full_size(oracle):
+    """All-to-all, W=8, 4096x4096 f16 blocks (256 MB input per member), 148 programs."""
+    import gemm_gather_gb300 as gg
+    W, M, N, dtype = 8, 4096, 4096, torch.float16
+    members = list(range(W))
+    blk_bytes = M * N * 2
+    in_off, out_off = GUARD, 2 * GUARD + W * blk_bytes
+    part = out_off + W * blk_bytes + GUARD
+    sh = _heap(W, part)
+    gen = gg_inputs.generator(1, device="cuda")
+    inputs = {}
+    for h in members:
+        x = gg_inputs.uniform_pm1((W * M, N), dtype, gen)
+        sh.view(h, in_off, W * M, N, N, dtype).copy_(x)
+        inputs[h] = x
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gg.all_to_all(sh.heap, -1, sh.ptr(0, in_off), N, sh.ptr(0, out_off), N, M, N, dtype, (8, 256),
+                  148, (0, 1, W), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    for d in members:
+        out = _ints(sh.view(d, out_off, W * M, N, N, dtype))
+        for i in members:
+            assert torch.equal(out[i * M:(i + 1) * M], _ints(inputs[i][d * M:(d + 1) * M])), (d, i)
+    for h in members:
+        p = sh.partition(h)
+        _assert_sentinel(p[:in_off], f"heap {h} front guard")
+        _assert_sentinel(p[in_off + W * blk_bytes:out_off], f"heap {h} middle guard")
+        _assert_sentinel(p[out_off + W * blk_bytes:], f"heap {h} back guard")
+    # sampled rows of every block against the oracle
+    rows = _rows_sample(M, 4, seed=7)
+    R = len(rows)
+    host_part = 2 * W * R * N * 2
+    img = np.full(W * host_part, gg_inputs.SENTINEL_BYTE, dtype=np.uint8)
+    idx_in = torch.from_numpy(np.concatenate([d * M + rows for d in range(W)])).cuda()
+    for h in members:
+        blk = _ints(inputs[h][idx_in]).cpu().numpy()
+        img[h * host_part: h * host_part + W * R * N * 2] = blk.view(np.uint8).ravel()
+    oracle.all_to_all(img, host_part, 0, N, W * R * N * 2, N, R, N, 2, (0, 1, W))
+    for d in members:
+        want = img[d * host_part + W * R * N * 2: (d + 1) * host_part].view(np.int16)
+        got = _ints(sh.view(d, out_off, W * M, N, N, dtype))[idx_in].cpu().numpy()
+        assert np.array_equal(got.ravel(), want), d
