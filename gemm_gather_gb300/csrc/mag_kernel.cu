@@ -37,9 +37,9 @@
 namespace gg {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, UK = 16;
-constexpr int kAStage = BM * BK * 2;            // 16 KB: 128 rows x 64 K, K-major
-constexpr int kBBox = BK * 64 * 2;              // 8 KB: 64 K-rows x 64 N-columns
+constexpr int BM = 128, BN = 256, UK = 16;
+constexpr int kKAtom = 64;                      // K elements of one 128-byte swizzle row
+constexpr int kAAtom = BM * kKAtom * 2;         // 16 KB: 128 rows x 64 K, K-major
 constexpr int kThreads = 192;                   // 6 warps
 constexpr int kTmemCols = 512;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
@@ -52,9 +52,13 @@ constexpr int kBox = 32 * 64 * 2;               // 4 KB: one epilogue store box,
 // tcgen05.mma.cta_group::2 over both CTAs' shared memory and TMEM.
 template <int CG>
 struct Geo {
+    // K depth of one ring stage: 64 (one swizzle atom of A) or 128 (two)
+    static constexpr int kBK = CG == 1 ? 64 : 64;
     static constexpr int kStages = CG == 1 ? 4 : 6;
-    static constexpr int kBCols = BN / CG;            // B columns one CTA holds
-    static constexpr int kBStage = BK * kBCols * 2;   // 32 KB or 16 KB
+    static constexpr int kAStage = BM * kBK * 2;       // A: kBK/64 atoms of 128 rows
+    static constexpr int kBBox = kBK * 64 * 2;         // B box: kBK K-rows x 64 N-columns
+    static constexpr int kBCols = BN / CG;             // B columns one CTA holds
+    static constexpr int kBStage = kBK * kBCols * 2;   // kBCols/64 boxes
     static constexpr int kTileM = BM * CG;            // rows of one (pair) tile
     // The epilogue stages each warp's 32 rows in column passes of kEpiCols,
     // as kEpiCols/64 swizzled boxes.
@@ -416,7 +420,7 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
     const int tiles_m = (int)((a.M + G::kTileM - 1) / G::kTileM);
     const int tiles_n = (int)((a.N + BN - 1) / BN);
     const int64_t total = (int64_t)a.n_src * tiles_m * tiles_n;
-    const int num_kb = (int)((a.K + BK - 1) / BK);
+    const int num_kb = (int)((a.K + G::kBK - 1) / G::kBK);
 
     // ---- prologue: barriers, TMEM, destination bases (loaded once) ----------
     if (threadIdx.x == 0) {
@@ -452,7 +456,7 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
         // ===================== producer =====================================
         const uint64_t pol_a = ptx::policy_evict_normal();  // A tile: read by tiles_n CTAs
         const uint64_t pol_b = ptx::policy_evict_last();    // B: read by every tile row
-        constexpr uint32_t kTx = CG * (kAStage + G::kBStage);  // bytes of one stage, both CTAs
+        constexpr uint32_t kTx = CG * (G::kAStage + G::kBStage);  // bytes of one stage, both CTAs
         int stage = 0;
         uint32_t phase = 0;
         int64_t issued = 0;
@@ -476,12 +480,16 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
                     const uint32_t bar = CG == 2 ? map_to_rank(local_full, 0) : local_full;
                     if (leader)
                         ptx::mbar_arrive_expect_tx(local_full, kTx);
-                    const uint32_t sa = base + G::kOffA + stage * kAStage;
+                    const uint32_t sa = base + G::kOffA + stage * G::kAStage;
                     const uint32_t sb = base + G::kOffB + stage * G::kBStage;
-                    tma_load_3d<CG>(sa, &map_a, kb * BK, row0, h_coord, bar, pol_a);
+#pragma unroll
+                    for (int ka = 0; ka < G::kBK / kKAtom; ++ka)
+                        tma_load_3d<CG>(sa + ka * kAAtom, &map_a, kb * G::kBK + ka * kKAtom, row0,
+                                        h_coord, bar, pol_a);
 #pragma unroll
                     for (int j = 0; j < G::kBCols / 64; ++j)
-                        tma_load_2d<CG>(sb + j * kBBox, &map_b, col0 + j * 64, kb * BK, bar, pol_b);
+                        tma_load_2d<CG>(sb + j * G::kBBox, &map_b, col0 + j * 64, kb * G::kBK, bar,
+                                        pol_b);
                 }
                 __syncwarp();
                 ++issued;
@@ -537,15 +545,18 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
                 }
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t sa = base + G::kOffA + stage * kAStage;
+                    const uint32_t sa = base + G::kOffA + stage * G::kAStage;
                     const uint32_t sb = base + G::kOffB + stage * G::kBStage;
 #pragma unroll
-                    for (int k = 0; k < BK / UK; ++k) {
-                        // A: K-major, +32 bytes per 16-element K step; SBO = 8 rows x 128 B
-                        const uint64_t ad = smem_desc(sa + k * (UK * 2), 16, 1024);
+                    for (int k = 0; k < G::kBK / UK; ++k) {
+                        // A: K-major, atom k/4, +32 bytes per 16-element K step inside the
+                        // 128-byte row; SBO = 8 rows x 128 B
+                        const uint32_t a_at =
+                            sa + (uint32_t)((k / (kKAtom / UK)) * kAAtom + (k % (kKAtom / UK)) * UK * 2);
+                        const uint64_t ad = smem_desc(a_at, 16, 1024);
                         // B: N-major, +16 K-rows x 128 B per K step; LBO = next 64-column
                         // box, SBO = 8 K-rows x 128 B
-                        const uint64_t bd = smem_desc(sb + k * (UK * 128), kBBox, 1024);
+                        const uint64_t bd = smem_desc(sb + k * (UK * 128), G::kBBox, 1024);
                         mma_f16<CG>(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
                     }
                     mma_commit_all<CG>(ptx::smem_addr(&sh.empty[stage]));
@@ -715,23 +726,24 @@ cudaError_t launch_matmul_all_gather(const FusedArgs &a, const OutMaps &out, int
                                   (uint64_t)(group ? a.num_heaps : 1)};
         const uint64_t strides[2] = {(uint64_t)a.lda * 2,
                                      group ? a.part_bytes : (uint64_t)(a.M * a.lda * 2)};
-        const uint32_t box[3] = {BK, BM, 1};
+        const uint32_t box[3] = {kKAtom, BM, 1};
         if (!encode_map(&map_a, dt, 3, ga, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) {
             *why = "encoding the tensor map of A";
             return cudaErrorInvalidValue;
         }
     }
+    const bool two_sm = variant != 1 && programs >= 2;
+    const int bk = two_sm ? Geo<2>::kBK : Geo<1>::kBK;  // K rows of one B box
     {
         const uint64_t dims[2] = {(uint64_t)a.N, (uint64_t)a.K};
         const uint64_t strides[1] = {(uint64_t)a.ldb * 2};
-        const uint32_t box[2] = {64, BK};
+        const uint32_t box[2] = {64, (uint32_t)bk};
         if (!encode_map(&map_b, dt, 2, a.b, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) {
             *why = "encoding the tensor map of B";
             return cudaErrorInvalidValue;
         }
     }
     const int64_t tiles_n = (a.N + BN - 1) / BN;
-    const bool two_sm = variant != 1 && programs >= 2;
     cudaError_t e;
     if (two_sm) {
         const int64_t pairs = (int64_t)a.n_src * ((a.M + 2 * BM - 1) / (2 * BM)) * tiles_n;
