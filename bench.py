@@ -418,6 +418,24 @@ def setup_device(dev, g: GatherCfg | None, f: FusedCfg | None, device_inputs: bo
     return sh, offs, Bd, host
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The slowest rank's value (replicas: the job is as slow as its slowest
+    GPU).  A no-op without an initialised process group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(roof_step_s: float, ms_per_step: float, world: int) -> float:
+    """Percent of one GPU's step roofline, summed over `world` replicas that
+    each ran the whole step in the (max-over-ranks) measured time."""
+    return 100.0 * world * roof_step_s / (ms_per_step * 1e-3)
+
+
 def sweep_points(name: str):
     """(GatherCfg | None, FusedCfg | None) points of the configuration sweeps."""
     pts = []
@@ -486,6 +504,8 @@ def run_sweep(args):
     torch.cuda.set_device(dev)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     for g, f in sweep_points(args.sweep):
+        if args.only and not any(o in (g or f).describe() for o in args.only.split("|")):
+            continue
         # --gather / --fused overrides apply to every point of the sweep
         g = parse_cfg(args.gather, g) if g else None
         f = parse_cfg(args.fused, f) if f else None
@@ -558,6 +578,8 @@ def main():
     ap.add_argument("--clocks-out", default=None)
     ap.add_argument("--sweep", default=None, choices=["budget", "gather", "fused", "variants"],
                     help="time every point of a configuration sweep (one JSON line each)")
+    ap.add_argument("--only", default="", help="sweep: run only points whose description "
+                    "contains one of these '|'-separated substrings")
     ap.add_argument("--sweep-clocks", action="store_true",
                     help="sample SM clocks while each sweep point runs (about 1 s per point)")
     args = ap.parse_args()
@@ -595,6 +617,16 @@ def main():
     gdt = gg_inputs.DTYPES[g.dtype] if g else None
     g_in_rows = (g.W * g.M if g.kind == "all_to_all" else g.M) if g else 0
     fdt = gg_inputs.DTYPES[f.dtype] if f else None
+
+    def launch_step(heap, b_dev, strm):
+        """The two kernels of one step on `heap` (a SymmetricHeap) and stream `strm`."""
+        if g:
+            launch_gather(gg, g, heap, offs, status, gdt, strm)
+        if f:
+            gg.matmul_all_gather(heap.heap, -1, heap.ptr(f.start, offs["f_a"]), f.K, b_dev, f.N,
+                                 heap.ptr(f.start, offs["f_out"]), f.N, f.M, f.N, f.K, fdt,
+                                 gg.FUSED_TILE, f.programs, (f.start, f.stride, f.W),
+                                 status=status, stream=strm, path=f.path)
 
     def step(ev=None):
         if ev is not None:
@@ -637,10 +669,7 @@ def main():
     elapsed_ms = t_start.elapsed_time(t_end)
     g_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) if g else 0.0
     f_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) if f else 0.0
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
     ms_step = elapsed_ms / args.steps
 
     # ---- end to end through the C ABI, host buffers, copies in the timed region
@@ -657,57 +686,127 @@ def main():
                 host["B"] = Bd.cpu()
         pin = {k: {h: x.pin_memory() for h, x in v.items()} for k, v in host.items() if k != "B"}
         pin_b = host["B"].pin_memory() if f else None
-        out_g = {h: torch.empty((g.W * g.M, g.N), dtype=gdt).pin_memory()
-                 for h in g.members()} if g else {}
-        out_f = {h: torch.empty((f.W * f.M, f.N), dtype=fdt).pin_memory()
-                 for h in f.members()} if f else {}
+
+        # The step's result: the gathered outputs.  Every member holds an identical
+        # copy (what the parity tests check), so the result is read from the first
+        # member; the variant that reads all W copies is timed as well.
+        def out_set(members_g, members_f):
+            og = {h: torch.empty((g.W * g.M, g.N), dtype=gdt).pin_memory()
+                  for h in members_g}
+            of = {h: torch.empty((f.W * f.M, f.N), dtype=fdt).pin_memory()
+                  for h in members_f}
+            return og, of
+
+        first_g = g.members()[:1] if g else []
+        first_f = f.members()[:1] if f else []
+        outs = [out_set(first_g, first_f), out_set(first_g, first_f)]
+        outs_all = [out_set(g.members() if g else [], f.members() if f else [])] * 2
         h2d = sum(x.numel() * x.element_size() for v in pin.values() for x in v.values()) + \
             (pin_b.numel() * 2 if f else 0)
-        d2h = sum(x.numel() * x.element_size() for x in list(out_g.values()) + list(out_f.values()))
 
-        def e2e_step():
+        def nbytes(oset):
+            return sum(x.numel() * x.element_size() for d in oset for x in d.values())
+
+        d2h = nbytes(outs[0])
+        d2h_all = nbytes(outs_all[0])
+
+        def copy_in(heap, b_dev):
             if g:
                 for h in g.members():
-                    sh.view(h, offs["g_in"], g_in_rows, g.N, g.N, gdt).copy_(pin["g_in"][h],
-                                                                              non_blocking=True)
+                    heap.view(h, offs["g_in"], g_in_rows, g.N, g.N, gdt).copy_(pin["g_in"][h],
+                                                                                non_blocking=True)
             if f:
                 for h in f.members():
-                    sh.view(h, offs["f_a"], f.M, f.K, f.K, fdt).copy_(pin["f_a"][h],
-                                                                       non_blocking=True)
-                Bd.copy_(pin_b, non_blocking=True)
-            step()
-            for h, o in out_g.items():
-                o.copy_(sh.view(h, offs["g_out"], g.W * g.M, g.N, g.N, gdt), non_blocking=True)
-            for h, o in out_f.items():
-                o.copy_(sh.view(h, offs["f_out"], f.W * f.M, f.N, f.N, fdt), non_blocking=True)
+                    heap.view(h, offs["f_a"], f.M, f.K, f.K, fdt).copy_(pin["f_a"][h],
+                                                                         non_blocking=True)
+                b_dev.copy_(pin_b, non_blocking=True)
+
+        def copy_out(heap, oset):
+            og, of = oset
+            for h, o in og.items():
+                o.copy_(heap.view(h, offs["g_out"], g.W * g.M, g.N, g.N, gdt), non_blocking=True)
+            for h, o in of.items():
+                o.copy_(heap.view(h, offs["f_out"], f.W * f.M, f.N, f.N, fdt), non_blocking=True)
 
         e2e_steps = max(1, min(args.e2e_steps, args.steps))
+
+        # (1) serial: copy in, compute, copy out, one step after the other, one stream
+        def serial_step():
+            copy_in(sh, Bd)
+            launch_step(sh, Bd, stream)
+            copy_out(sh, outs[0])
+
         for _ in range(3):
-            e2e_step()
+            serial_step()
         barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(e2e_steps):
-            e2e_step()
+            serial_step()
         e1.record(stream)
         barrier()
-        e2e_ms = e0.elapsed_time(e1) / e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        serial_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
+
+        # (2) pipelined: two device buffer sets; step i copies in on one stream,
+        # computes on another and copies out on a third, overlapping steps i-1
+        # and i+1 (every step still moves all of its inputs and outputs)
+        sh2 = gg.SymmetricHeap(sh.H, sh.part_bytes, device=dev)
+        bufs = [(sh, Bd), (sh2, torch.empty_like(Bd) if f else None)]
+        s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_cmp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+
+        def pipelined(n, out_sets):
+            for i in range(n):
+                b = i % 2
+                heap, b_dev = bufs[b]
+                with torch.cuda.stream(s_in):
+                    if i >= 2:
+                        s_in.wait_event(ev_cmp[b])  # step i-2 no longer reads these inputs
+                    copy_in(heap, b_dev)
+                    ev_in[b].record(s_in)
+                with torch.cuda.stream(s_cmp):
+                    s_cmp.wait_event(ev_in[b])
+                    if i >= 2:
+                        s_cmp.wait_event(ev_out[b])  # step i-2's outputs are copied out
+                    launch_step(heap, b_dev, s_cmp)
+                    ev_cmp[b].record(s_cmp)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_cmp[b])
+                    copy_out(heap, out_sets[b])
+                    ev_out[b].record(s_out)
+
+        def timed_pipeline(out_sets):
+            pipelined(3, out_sets)
+            barrier()
+            p0 = torch.cuda.Event(enable_timing=True)
+            p1 = torch.cuda.Event(enable_timing=True)
+            p0.record(s_in)
+            pipelined(e2e_steps, out_sets)
+            p1.record(s_out)
+            barrier()
+            return max_over_ranks(p0.elapsed_time(p1) / e2e_steps, dev)
+
+        e2e_ms = timed_pipeline(outs)
+        all_ms = timed_pipeline(outs_all)
         e2e = {"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "steps": e2e_steps,
-               "path": "pinned host -> heap (cudaMemcpyAsync) -> C-ABI calls -> pinned host"}
+               "steps": e2e_steps, "serial_ms_per_step": serial_ms,
+               "all_copies": {"d2h_bytes_per_step": d2h_all, "ms_per_step": all_ms},
+               "path": ("pinned host -> heap (cudaMemcpyAsync) -> C-ABI calls -> pinned host; "
+                        "every member's inputs copied in, the gathered outputs read back from "
+                        "member 0 (all members hold identical copies); steps pipelined over two "
+                        "device buffer sets and three streams; all_copies reads every member's "
+                        "output")}
+        del sh2, bufs
 
     # ---- roofline bookkeeping
     t_rg, t_rf = roofline_times(peaks, g, f)
     roof_step = t_rg + t_rf
-    value = 100.0 * world * roof_step / (ms_step * 1e-3)
+    value = whole_job_value(roof_step, ms_step, world)
     if e2e:
-        e2e = {"value": 100.0 * world * roof_step / (e2e["ms_per_step"] * 1e-3), "unit": UNIT,
-               **e2e}
+        e2e = {"value": whole_job_value(roof_step, e2e["ms_per_step"], world), "unit": UNIT, **e2e}
     hbm_peak = peaks["hbm_gbs"]
     tc_peak = peaks["bf16_tflops"] * F16_PER_BF16
     kernels = {}
