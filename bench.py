@@ -456,6 +456,9 @@ def sweep_points(name: str):
             for N in (4096, 8192):
                 pts.append((GatherCfg(W=4, M=M, N=N, dtype="f16", start=1, stride=2,
                                       values="normal"), None))
+    elif name == "small":  # the 2-rank 64x256 f16 case, tile 8x256, 4 programs: launch-bound
+        for path in ("tma", "bulk", "vector"):
+            pts.append((GatherCfg(W=2, M=64, N=256, programs=4, path=path), None))
     elif name == "variants":  # partitioned all-gather, destination grouping, all-to-all
         for p in (8, 16, 32, 64, 148):
             pts.append((replace(GATHER, programs=p, kind="partitioned", path="tma"), None))
@@ -545,6 +548,23 @@ def run_sweep(args):
             raise RuntimeError(f"device status {int(status.item())}")
         rec = {"sweep": args.sweep, "workload": (g or f).describe(), "ms": ms, "steps": steps,
                "roofline_ms": 1e3 * work, "frac": 1e3 * work / ms}
+        if args.sweep == "small":
+            # the same launches replayed from a CUDA graph (no per-launch host work)
+            cap = torch.cuda.Stream(dev)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=cap):
+                for _ in range(100):
+                    launch()
+            graph.replay()
+            torch.cuda.synchronize(dev)
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g0.record()
+            for _ in range(10):
+                graph.replay()
+            g1.record()
+            torch.cuda.synchronize(dev)
+            rec["us_per_launch"] = 1e3 * ms
+            rec["graph_us_per_launch"] = g0.elapsed_time(g1) / 1000 * 1e3
         if clk:
             rec["clocks"] = clk
             if f:
@@ -576,7 +596,8 @@ def main():
     ap.add_argument("--device-inputs", default="auto", choices=["auto", "yes", "no"],
                     help="draw inputs on the GPU (seeded) instead of the CPU")
     ap.add_argument("--clocks-out", default=None)
-    ap.add_argument("--sweep", default=None, choices=["budget", "gather", "fused", "variants"],
+    ap.add_argument("--sweep", default=None,
+                    choices=["budget", "gather", "fused", "variants", "small"],
                     help="time every point of a configuration sweep (one JSON line each)")
     ap.add_argument("--only", default="", help="sweep: run only points whose description "
                     "contains one of these '|'-separated substrings")

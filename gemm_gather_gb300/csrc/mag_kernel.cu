@@ -31,6 +31,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "gg_internal.h"
 #include "ptx.cuh"
 
@@ -63,6 +65,13 @@ struct Geo {
     // The epilogue stages each warp's 32 rows in column passes of kEpiCols,
     // as kEpiCols/64 swizzled boxes.
     static constexpr int kEpiCols = CG == 1 ? 64 : 128;
+    // Epilogue stores: TMA tensor stores of the staged boxes (false), or
+    // 16-byte vector stores read back from the staged boxes (true).
+    static constexpr bool kEpiVector = false;
+    // Each tile walks its K blocks cyclically from a per-tile starting block,
+    // so tiles sharing an A row block or a B column block do not request the
+    // same slice at the same moment (the f32 accumulation order changes).
+    static constexpr bool kKRotate = false;
     static constexpr int kEpiBoxes = kEpiCols / 64;
     static constexpr int kEpiWarp = kEpiBoxes * kBox;  // one epilogue warp's staging
     static constexpr int kOffA = 0;
@@ -77,6 +86,7 @@ struct FusedShared {
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t mma_done;
+    uint64_t dst[kMaxWorld];  // output base of member i (vector-store epilogue)
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -347,6 +357,24 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi, int bf16)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// Streaming (evict-first) 16-byte global store.
+__device__ __forceinline__ void st_global_cs_v4(void *p, uint4 v)
+{
+    asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d)
 {
@@ -444,8 +472,12 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
         tmem_alloc<CG>(ptx::smem_addr(&sh.tmem_base));
         tc_fence_before();
     }
-    if (threadIdx.x < (unsigned)a.W)
+    if (threadIdx.x < (unsigned)a.W) {
         prefetch_tensormap(&out.map[threadIdx.x]);
+        // heap bases -> member output bases, once, before any tile
+        sh.dst[threadIdx.x] =
+            a.bases[a.rank_start + threadIdx.x * a.rank_stride] + (uint64_t)a.out_off;
+    }
     __syncthreads();
     if constexpr (CG == 2)
         cluster_sync();  // the peer's barriers exist before anything signals them
@@ -466,7 +498,12 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
             const int h_coord = a.a_abs ? 0 : c.h;
             const int row0 = c.tm * G::kTileM + (int)rank * BM;
             const int col0 = c.tn * BN + (int)rank * G::kBCols;
+            const int k_first =
+                G::kKRotate ? (int)(((int64_t)c.tm * 7 + (int64_t)c.tn * 3 + c.g * 5) % num_kb) : 0;
             for (int kb = 0; kb < num_kb; ++kb) {
+                int kq = kb + k_first;  // the K block this stage carries
+                if (kq >= num_kb)
+                    kq -= num_kb;
                 const bool got = role_wait(ptx::smem_addr(&sh.empty[stage]), phase ^ 1u,
                                            a.wait_limit_ns, abort_flag);
                 if (!__all_sync(0xffffffffu, got)) {
@@ -484,11 +521,11 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
                     const uint32_t sb = base + G::kOffB + stage * G::kBStage;
 #pragma unroll
                     for (int ka = 0; ka < G::kBK / kKAtom; ++ka)
-                        tma_load_3d<CG>(sa + ka * kAAtom, &map_a, kb * G::kBK + ka * kKAtom, row0,
+                        tma_load_3d<CG>(sa + ka * kAAtom, &map_a, kq * G::kBK + ka * kKAtom, row0,
                                         h_coord, bar, pol_a);
 #pragma unroll
                     for (int j = 0; j < G::kBCols / 64; ++j)
-                        tma_load_2d<CG>(sb + j * G::kBBox, &map_b, col0 + j * 64, kb * G::kBK, bar,
+                        tma_load_2d<CG>(sb + j * G::kBBox, &map_b, col0 + j * 64, kq * G::kBK, bar,
                                         pol_b);
                 }
                 __syncwarp();
@@ -653,9 +690,43 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
                     }
                 }
                 // staged boxes -> every destination, local first, peers rotated
+                const int col0 = c.tn * BN + pass;
+                if constexpr (G::kEpiVector) {
+                    __syncwarp();  // every row of the boxes is staged
+                    const int64_t ld_out_b = a.ld_out * 2;
+#pragma unroll 1
+                    for (int b = 0; b < G::kEpiBoxes; ++b) {
+                        const int colb = col0 + b * 64;
+                        if (colb >= a.N)
+                            break;
+                        const uint32_t box = warp_stage + (uint32_t)(b * kBox);
+#pragma unroll 2
+                        for (int it = 0; it < 8; ++it) {
+                            // 16-byte chunk: row r of the box, columns 8k..8k+7
+                            const int ch = it * 32 + lane;
+                            const int r = ch >> 3, k = ch & 7;
+                            const uint4 v = ld_shared_v4(box + (uint32_t)(r * 128) +
+                                                         ((uint32_t)(k ^ (r & 7)) << 4));
+                            const int64_t row = (int64_t)row0 + r;
+                            const int col = colb + k * 8;
+                            if (row < a.M && col < a.N) {
+                                const int64_t off = ((int64_t)c.g * a.M + row) * ld_out_b +
+                                                    (int64_t)col * 2;
+                                for (int j = 0; j < a.W; ++j) {
+                                    int i = c.g + j;
+                                    if (i >= a.W)
+                                        i -= a.W;
+                                    st_global_cs_v4(reinterpret_cast<uint8_t *>(sh.dst[i]) + off,
+                                                    v);
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();  // the boxes may be restaged
+                    continue;
+                }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
-                const int col0 = c.tn * BN + pass;
                 if (row0 < a.M) {
                     for (int op = lane; op < a.W * kOps; op += 32) {
                         const int j = op / kOps;
@@ -754,24 +825,32 @@ cudaError_t launch_matmul_all_gather(const FusedArgs &a, const OutMaps &out, int
             return e;
         }
         // persistent pairs: never more clusters than can be resident at once
-        int resident = 0;
-        {
+        // (queried once per device; later calls, e.g. under stream capture,
+        // reuse the answer)
+        static int resident_by_dev[64];
+        static std::once_flag once_by_dev[64];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+            dev = 0;
+        std::call_once(once_by_dev[dev], [&] {
+            int resident = 0;
             cudaLaunchConfig_t cfg = {};
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
             attr[0].val.clusterDim.x = 2;
             attr[0].val.clusterDim.y = 1;
             attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3(2 * (unsigned)gg_min64(programs / 2, pairs), 1, 1);
+            cfg.gridDim = dim3(2, 1, 1);
             cfg.blockDim = dim3(kThreads, 1, 1);
             cfg.dynamicSmemBytes = smem_bytes<2>();
-            cfg.stream = s;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             if (cudaOccupancyMaxActiveClusters(&resident, mag2_kernel, &cfg) != cudaSuccess)
                 resident = 0;
             (void)cudaGetLastError();
-        }
+            resident_by_dev[dev] = resident;
+        });
+        const int resident = resident_by_dev[dev];
         int64_t clusters = gg_min64(programs / 2, pairs);
         if (resident > 0)
             clusters = gg_min64(clusters, resident);
