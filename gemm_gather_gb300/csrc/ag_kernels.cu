@@ -55,6 +55,9 @@ constexpr int kAgWarps = 8;           // most independent pipelines (warps) per 
 // kAgTargetPipes / programs of them (1..kAgWarps), so a small budget still
 // keeps enough copies in flight and a large one does not oversubscribe.
 constexpr int kAgTargetPipes = 512;
+// The partitioned gather and the all-to-all store each tile once (not W
+// times), so a pipeline moves W times fewer bytes per load: they aim higher.
+constexpr int kAgTargetPipesSingle = 2048;
 constexpr int kAgMaxStages = 16;      // ring stages per pipeline
 constexpr int kAgSmemBudget = 192 * 1024;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;  // waits for copies already in flight
@@ -474,11 +477,11 @@ __global__ void __launch_bounds__(kVecThreads) ag_vec_kernel(const GatherArgs a)
 // Ring geometry for a tile of `stage_raw` bytes and `programs` programs:
 // pipelines (warps) per program, stages per pipeline and read depth D.
 // False if not even one pipeline of three stages fits.
-bool ring_geometry(int64_t stage_raw, int programs, int *npipe, int *stages, int *depth,
-                   int *stage_bytes)
+bool ring_geometry(int64_t stage_raw, int programs, int target, int *npipe, int *stages,
+                   int *depth, int *stage_bytes)
 {
     const int64_t sb = (stage_raw + 1023) / 1024 * 1024;
-    int want = (kAgTargetPipes + programs - 1) / programs;
+    int want = (target + programs - 1) / programs;
     want = want < 1 ? 1 : (want > kAgWarps ? kAgWarps : want);
     for (int np = want; np >= 1; --np) {
         const int64_t st = gg_min64(kAgMaxStages, (kAgSmemBudget - kAgHeader) / (np * sb));
@@ -524,7 +527,9 @@ cudaError_t launch_gather_tma(const CUtensorMap &in_map, const OutMaps &out, con
                               int programs, cudaStream_t s)
 {
     int npipe, stages, depth, stage_bytes;
-    if (!ring_geometry((int64_t)a.bm * a.bn_b, programs, &npipe, &stages, &depth, &stage_bytes))
+    const int target = a.mode == kModeGather ? kAgTargetPipes : kAgTargetPipesSingle;
+    if (!ring_geometry((int64_t)a.bm * a.bn_b, programs, target, &npipe, &stages, &depth,
+                       &stage_bytes))
         return cudaErrorInvalidValue;
     switch (depth) {
     case 4: return launch_tma_depth<4>(in_map, out, a, programs, npipe, stages, stage_bytes, s);
@@ -536,7 +541,8 @@ cudaError_t launch_gather_tma(const CUtensorMap &in_map, const OutMaps &out, con
 cudaError_t launch_gather_bulk(const GatherArgs &a, int programs, cudaStream_t s)
 {
     int npipe, stages, depth, stage_bytes;
-    if (!ring_geometry((int64_t)a.bm * a.bn_b, programs, &npipe, &stages, &depth, &stage_bytes))
+    if (!ring_geometry((int64_t)a.bm * a.bn_b, programs, kAgTargetPipes, &npipe, &stages, &depth,
+                       &stage_bytes))
         return cudaErrorInvalidValue;  // tile too large (the host validates first)
     switch (depth) {
     case 4: return launch_bulk_depth<4>(a, programs, npipe, stages, stage_bytes, s);
