@@ -4,7 +4,7 @@
 One step = one pass of the whole path over one batch of synthetic inputs:
   1. persistent all-gather: W=8 logical ranks, 4096 x 4096 f16 per rank
      (uniform[-1,1]), explicit tile 8x256, 148 programs, local copy first
-     then peers rotated;
+     then peers rotated (tensor-map path, runs of tiles claimed per program);
   2. fused matmul + all-gather: W=8, M_local=1024, N=3584, K=8192, f16 in,
      f32 accumulate, f16 out, 128x256 tcgen05 tiles, inputs normal(0,1)/sqrt(K).
 Every rank's 8 logical ranks live in one symmetric heap on its own GPU; the
@@ -90,11 +90,10 @@ class FusedCfg:
 
 
 ES = {"f16": 2, "bf16": 2, "f32": 4}
-# The benchmark's all-gather runs the bulk-copy path: at 148 programs with
-# 8x256 tiles it measured about 5% faster than the tensor-map path, which the
-# library's automatic choice prefers (it wins at smaller budgets and most
-# other shapes; see the sweeps).
-GATHER = GatherCfg(path="bulk")
+# The benchmark's all-gather takes the library's automatic choice: the
+# tensor-map path, which at 148 programs claims runs of tiles from the heap's
+# workspace (load balancing across SMs).
+GATHER = GatherCfg()
 FUSED = FusedCfg()
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -502,6 +501,8 @@ def run_sweep(args):
 
     import gemm_gather_gb300 as gg
     import gg_inputs
+    if args.claims is not None:
+        gg.set_claim_policy(args.claims)
     peaks, peak_src = load_peaks()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
@@ -603,6 +604,9 @@ def main():
                     "contains one of these '|'-separated substrings")
     ap.add_argument("--sweep-clocks", action="store_true",
                     help="sample SM clocks while each sweep point runs (about 1 s per point)")
+    ap.add_argument("--claims", default=None, choices=["auto", "always", "never"],
+                    help="which gather launches claim runs of tiles from the heap's workspace "
+                    "(default: the library's, auto)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.sweep:
@@ -619,6 +623,8 @@ def main():
     import gemm_gather_gb300 as gg
     import gg_inputs
 
+    if args.claims is not None:
+        gg.set_claim_policy(args.claims)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

@@ -18,12 +18,16 @@ from ._lib import (GG_AG_AUTO, GG_AG_BULK, GG_AG_TMA, GG_AG_VECTOR, GG_BF16, GG_
                    GG_COLL_ALL_TO_ALL, GG_ERR_ALIGNMENT,
                    GG_ERR_CUDA, GG_ERR_INVALID_ARG, GG_ERR_NOT_IN_HEAP, GG_ERR_TIMEOUT,
                    GG_ERR_UNSUPPORTED, GG_F16, GG_F32, GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N,
-                   GG_MAX_WORLD, GG_OK, GGError, Group, Tile, check, lib, LIB_PATH)
+                   GG_CLAIM_ALWAYS, GG_CLAIM_AUTO, GG_CLAIM_NEVER, GG_MAX_WORLD, GG_OK,
+                   GG_WORKSPACE_SLOT_BYTES,
+                   GGError, Group, Tile, check, lib, LIB_PATH)
 
 __all__ = [
-    "heap_create", "heap_wrap", "heap_bases", "heap_info", "heap_destroy", "all_gather",
+    "heap_create", "heap_wrap", "heap_bases", "heap_info", "heap_destroy", "heap_set_workspace",
+    "all_gather",
     "all_gather_check", "all_gather_grouped", "all_gather_partitioned", "all_to_all",
-    "collective_check", "matmul_all_gather", "matmul_all_gather_check", "set_wait_limit_ns",
+    "collective_check", "matmul_all_gather", "matmul_all_gather_check", "set_claim_policy",
+    "get_claim_policy", "CLAIM_POLICIES", "set_wait_limit_ns",
     "get_wait_limit_ns", "debug_inject_stall", "SymmetricHeap", "Heap", "GGError", "DTYPE_CODES", "PATHS",
     "FUSED_TILE", "FUSED_PATHS",
 ]
@@ -32,6 +36,7 @@ DTYPE_CODES = {torch.float16: GG_F16, torch.bfloat16: GG_BF16, torch.float32: GG
 PATHS = {"auto": GG_AG_AUTO, "bulk": GG_AG_BULK, "vector": GG_AG_VECTOR, "tma": GG_AG_TMA}
 FUSED_PATHS = {"auto": GG_MAG_AUTO, "1sm": GG_MAG_1SM, "2sm": GG_MAG_2SM}
 FUSED_TILE = (GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N)
+CLAIM_POLICIES = {"auto": GG_CLAIM_AUTO, "always": GG_CLAIM_ALWAYS, "never": GG_CLAIM_NEVER}
 
 
 def _ptr(x) -> int | None:
@@ -106,6 +111,11 @@ def heap_destroy(heap: Heap) -> None:
     if heap.handle:
         check(lib.gg_heap_destroy(heap.handle))
         heap.handle = None
+
+
+def heap_set_workspace(heap: Heap, dev_work, nbytes: int) -> None:
+    """Workspace for load-balanced launches (``dev_work`` None and 0 bytes: none)."""
+    check(lib.gg_heap_set_workspace(heap.handle, _ptr(dev_work), nbytes))
 
 
 def all_gather(heap: Heap, rank: int, input, ld_in: int, output, ld_out: int, M: int, N: int,
@@ -192,6 +202,17 @@ def matmul_all_gather_check(heap: Heap, rank: int, A, lda: int, B, ldb: int, out
                                          Tile(*tile), comm_programs, Group(*group)))
 
 
+def set_claim_policy(policy: str) -> None:
+    """Which launches claim runs of tiles from the heap's workspace:
+    "auto", "always" or "never"."""
+    check(lib.gg_set_claim_policy(CLAIM_POLICIES[policy]))
+
+
+def get_claim_policy() -> str:
+    code = int(lib.gg_get_claim_policy())
+    return next(k for k, v in CLAIM_POLICIES.items() if v == code)
+
+
 def set_wait_limit_ns(ns: int) -> None:
     check(lib.gg_set_wait_limit_ns(ns))
 
@@ -215,7 +236,7 @@ class SymmetricHeap:
     ALIGN = 256
 
     def __init__(self, num_heaps: int, part_bytes: int, device="cuda", fill: int | None = None,
-                 stream=None):
+                 stream=None, workspace_slots: int = 64):
         if part_bytes % self.ALIGN:
             part_bytes += self.ALIGN - part_bytes % self.ALIGN
         self.H = num_heaps
@@ -228,6 +249,15 @@ class SymmetricHeap:
             self.storage.fill_(fill)
         self.table = torch.empty(num_heaps, dtype=torch.int64, device=device)
         self.heap = heap_create(self.storage, part_bytes, num_heaps, self.table, stream=stream)
+        # load-balancing counters (each launch that uses a slot zeroes it first)
+        self.workspace = None
+        if workspace_slots:
+            nbytes = workspace_slots * GG_WORKSPACE_SLOT_BYTES
+            ws = torch.zeros(nbytes + self.ALIGN, dtype=torch.uint8, device=device)
+            shift = (-ws.data_ptr()) % self.ALIGN
+            self._ws_raw = ws
+            self.workspace = ws[shift: shift + nbytes]
+            heap_set_workspace(self.heap, self.workspace, nbytes)
 
     @property
     def base(self) -> int:

@@ -26,13 +26,17 @@ GG_COLL_ALL_GATHER, GG_COLL_ALL_GATHER_PARTITIONED, GG_COLL_ALL_TO_ALL = 0, 1, 2
 GG_MAX_WORLD = 64
 GG_MAX_HEAPS = 1024
 GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N = 128, 256
+GG_WORKSPACE_SLOT_BYTES = 128
+GG_CLAIM_AUTO, GG_CLAIM_ALWAYS, GG_CLAIM_NEVER = 0, 1, 2
 
 # Every entry point declared in include/gemm_gather.h.
 EXPORTS = (
     "gg_heap_create", "gg_heap_wrap", "gg_heap_bases", "gg_heap_info", "gg_heap_destroy",
+    "gg_heap_set_workspace",
     "gg_all_gather", "gg_all_gather_path", "gg_all_gather_check", "gg_all_gather_grouped",
     "gg_all_gather_partitioned", "gg_all_to_all", "gg_collective_check",
     "gg_matmul_all_gather", "gg_matmul_all_gather_path", "gg_matmul_all_gather_check",
+    "gg_set_claim_policy", "gg_get_claim_policy",
     "gg_set_wait_limit_ns", "gg_get_wait_limit_ns", "gg_debug_inject_stall",
     "gg_last_error", "gg_status_string", "gg_version",
 )
@@ -57,6 +61,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "gg_heap_bases": ([vp, ctypes.POINTER(u64), i32], i32),
         "gg_heap_info": ([vp, ctypes.POINTER(i32), ctypes.POINTER(sz)], i32),
         "gg_heap_destroy": ([vp], i32),
+        "gg_heap_set_workspace": ([vp, vp, sz], i32),
         "gg_all_gather": ([vp, i32, vp, i64, vp, i64, i64, i64, i32, Tile, i32, Group, vp, vp],
                           i32),
         "gg_all_gather_path": ([vp, i32, vp, i64, vp, i64, i64, i64, i32, Tile, i32, Group, vp,
@@ -77,6 +82,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
                                        Tile, i32, Group, vp, vp, i32], i32),
         "gg_matmul_all_gather_check": ([vp, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, i32,
                                         Tile, i32, Group], i32),
+        "gg_set_claim_policy": ([i32], i32),
+        "gg_get_claim_policy": ([], i32),
         "gg_set_wait_limit_ns": ([u64], i32),
         "gg_get_wait_limit_ns": ([], u64),
         "gg_debug_inject_stall": ([i32], i32),

@@ -62,14 +62,6 @@ constexpr int kAgMaxStages = 16;      // ring stages per pipeline
 constexpr int kAgSmemBudget = 192 * 1024;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;  // waits for copies already in flight
 
-struct AgShared {
-    uint64_t full[kAgWarps][kAgMaxStages];  // one mbarrier per ring stage
-    uint64_t dst[kMaxWorld];                // output base of member i
-    uint64_t src[kMaxWorld];                // input base of member i
-};
-
-constexpr int kAgHeader = (int)((sizeof(AgShared) + 127) / 128 * 128);
-
 struct Item {
     int g;          // group index of the source
     int d;          // group index of the destination block (all-to-all), else -1
@@ -77,6 +69,15 @@ struct Item {
     int rows;       // valid rows of the tile
     uint32_t rb;    // valid bytes per tile row
 };
+
+struct AgShared {
+    uint64_t full[kAgWarps][kAgMaxStages];  // one mbarrier per ring stage
+    Item item[kAgWarps][kAgMaxStages];      // the tile a ring stage holds (decoded at issue)
+    uint64_t dst[kMaxWorld];                // output base of member i
+    uint64_t src[kMaxWorld];                // input base of member i
+};
+
+constexpr int kAgHeader = (int)((sizeof(AgShared) + 127) / 128 * 128);
 
 // The items one pipeline (warp) of a program walks: first, first + step, ...
 // and, for the partitioned all-gather, the one destination its program serves.
@@ -100,6 +101,100 @@ __device__ __forceinline__ Walk make_walk(const GatherArgs &a, int warp, int npi
     w.n = w.first < a.total_items ? (a.total_items - 1 - w.first) / w.step + 1 : 0;
     w.dest = dest;
     return w;
+}
+
+// The items one ring pipeline (warp) loads, in order.  With P pipelines
+// (of one destination for the partitioned all-gather), items are handed
+// out in runs: run n covers items b, b + P, b + 2P, ... (`chunk` of them, up to
+// the last item), where b = (n / P) * P * chunk + n % P.  Pipelines working
+// side by side therefore touch neighbouring tiles, as with fixed shares.
+//  * fixed shares (no counter): pipeline p takes run p, with no length limit:
+//    items p, p + P, p + 2P, ...;
+//  * claimed runs (counter): pipeline p takes run p (`chunk` items), then
+//    claims run P + (counter++) each time its run is done.  Programs on SMs
+//    that move data faster claim more runs, so all programs finish together
+//    whatever share of the memory system their SMs get.  Lane 0 keeps two
+//    claims in flight (q0, q1) so that a claim's latency hides behind the
+//    items before it.
+struct Feed {
+    int64_t cur;                // next item of the current run
+    int64_t left;               // items left in the current run
+    int64_t pipes, total;
+    unsigned long long *ctr;    // claimed runs: the counter; null: fixed shares
+    unsigned long long q0, q1;  // lane 0: the two claims in flight
+    int chunk;
+    int phase;                  // which claim is the older one
+    bool dry;                   // no item left
+};
+
+__device__ __forceinline__ Feed make_feed(const GatherArgs &a, int warp, int npipe, int lane,
+                                          int *dest)
+{
+    int64_t prog = blockIdx.x, nprog = gridDim.x;
+    int d = -1;
+    unsigned long long *ctr = a.work;
+    if (a.mode == kModePartitioned) {  // program p serves destination p mod W
+        d = (int)(blockIdx.x % (unsigned)a.W);
+        prog = blockIdx.x / (unsigned)a.W;
+        nprog = (gridDim.x - 1 - d) / a.W + 1;
+        ctr = nullptr;  // fixed shares (claims do not pay off here)
+    }
+    *dest = d;
+    Feed f;
+    f.pipes = nprog * npipe;
+    f.cur = prog + (int64_t)warp * nprog;
+    f.total = a.total_items;
+    f.ctr = ctr;
+    f.chunk = a.chunk;
+    f.left = ctr ? a.chunk : a.total_items;
+    f.phase = 0;
+    f.dry = false;
+    f.q0 = f.q1 = 0;
+    if (ctr && lane == 0 && f.pipes * a.chunk < a.total_items) {
+        f.q0 = atomicAdd(ctr, 1ull);
+        f.q1 = atomicAdd(ctr, 1ull);
+    }
+    return f;
+}
+
+// Next item of the pipeline, or -1.  Warp-uniform: every lane calls it.
+__device__ __forceinline__ int64_t feed_next(Feed &f, int lane)
+{
+    if (f.dry)
+        return -1;
+    if (f.left == 0 || f.cur >= f.total) {
+        if (!f.ctr || f.pipes * f.chunk >= f.total) {
+            f.dry = true;
+            return -1;
+        }
+        // take the older claim, put a new one in its place (each branch
+        // touches one claim register, so the newer claim is not waited for)
+        unsigned long long c;
+        if (f.phase == 0)
+            c = __shfl_sync(0xffffffffu, f.q0, 0);
+        else
+            c = __shfl_sync(0xffffffffu, f.q1, 0);
+        const int64_t n = f.pipes + (int64_t)c;
+        const int64_t b = n / f.pipes * f.pipes * f.chunk + n % f.pipes;
+        // b grows with n: once past the end, every later claim is too
+        if (b >= f.total) {
+            f.dry = true;
+            return -1;
+        }
+        if (lane == 0) {
+            if (f.phase == 0)
+                f.q0 = atomicAdd(f.ctr, 1ull);
+            else
+                f.q1 = atomicAdd(f.ctr, 1ull);
+        }
+        f.phase ^= 1;
+        f.cur = b;
+        f.left = f.chunk;
+    }
+    const int64_t t = f.cur;
+    f.cur += f.pipes;
+    --f.left;
+    return t;
 }
 
 // Item t: source-major; for the all-to-all each source's items run over its W
@@ -196,10 +291,8 @@ __global__ void __launch_bounds__(kAgWarps * 32)
     }
     __syncthreads();
 
-    // Items of this pipeline: blockIdx.x + (warp + npipe*k) * gridDim.x.
-    const int64_t step = (int64_t)gridDim.x * npipe;
-    const int64_t first = blockIdx.x + (int64_t)warp * gridDim.x;
-    const int64_t n_local = first < a.total_items ? (a.total_items - 1 - first) / step + 1 : 0;
+    int dest;
+    Feed feed = make_feed(a, warp, npipe, lane, &dest);
     const int lookahead = stages - D;  // loads in flight ahead of the stores
 
     const uint32_t ring = ptx::smem_addr(smem + kAgHeader) + (uint32_t)(warp * stages * stage_bytes);
@@ -207,12 +300,27 @@ __global__ void __launch_bounds__(kAgWarps * 32)
     const uint32_t pitch = (uint32_t)a.bn_b;  // staged row pitch (multiple of 16)
     const int grp = (a.dests_per_wait > 0 && a.dests_per_wait < a.W) ? a.dests_per_wait : a.W;
 
-    auto issue_load = [&](int64_t k) {
-        const Item it = decode_item(a, first + k * step);
-        const int st = (int)(k % stages);
+    // Takes the pipeline's next item (if any) and starts its load into ring
+    // slot `issued`.
+    int64_t issued = 0;
+    auto issue_next = [&]() {
+        const int64_t t = feed_next(feed, lane);
+        if (t < 0)
+            return;
+        if (issued >= stages) {
+            // the stage last held item issued - stages = (issued - lookahead) - D
+            ptx::bulk_wait_read<D>();
+            __syncwarp();
+        }
+        const Item it = decode_item(a, t);
+        const int st = (int)(issued % stages);
         const uint32_t bar = full0 + 8u * st;
         const uint32_t buf = ring + (uint32_t)st * stage_bytes;
-        if (a.inject_stall && k == 0 && blockIdx.x == 0 && warp == 0)
+        if (lane == 0)
+            sh.item[warp][st] = it;
+        const bool stall = a.inject_stall && issued == 0 && blockIdx.x == 0 && warp == 0;
+        ++issued;
+        if (stall)
             return;  // test hook: this stage's barrier phase never completes
         if (lane == 0)
             ptx::mbar_arrive_expect_tx(bar, (uint32_t)it.rows * it.rb);
@@ -223,13 +331,12 @@ __global__ void __launch_bounds__(kAgWarps * 32)
             ptx::bulk_g2s(buf + (uint32_t)r * pitch, src + r * a.ld_in_b, it.rb, bar);
     };
 
-    const int64_t preload = gg_min64(lookahead, n_local);
-    for (int64_t k = 0; k < preload; ++k)
-        issue_load(k);
+    for (int q = 0; q < lookahead; ++q)
+        issue_next();
 
     int64_t k = 0;
     bool ok = true;
-    for (; k < n_local; ++k) {
+    for (; k < issued; ++k) {
         const int st = (int)(k % stages);
         const uint32_t parity = (uint32_t)((k / stages) & 1);
         const bool mine = ptx::mbar_wait(full0 + 8u * st, parity, a.wait_limit_ns);
@@ -237,7 +344,7 @@ __global__ void __launch_bounds__(kAgWarps * 32)
             ok = false;
             break;
         }
-        const Item it = decode_item(a, first + k * step);
+        const Item it = sh.item[warp][st];
         const uint32_t buf = ring + (uint32_t)st * stage_bytes;
         const int64_t row0 = (int64_t)it.g * a.M + it.tm * a.bm;
         const int64_t col0 = it.tn * a.bn_b;
@@ -262,22 +369,14 @@ __global__ void __launch_bounds__(kAgWarps * 32)
                 __syncwarp();
             }
         }
-        const int64_t kk = k + lookahead;
-        if (kk < n_local) {
-            if (kk >= stages) {
-                // the stage of item kk last held item kk - stages = k - D
-                ptx::bulk_wait_read<D>();
-                __syncwarp();
-            }
-            issue_load(kk);
-        }
+        __syncwarp();  // every lane has read this stage's item
+        issue_next();
     }
 
     if (!ok) {
         report_status(a.status, kStatusTimeout);
-        // loads issued but not consumed: items k .. min(k + lookahead, n_local) - 1
-        const int64_t end = gg_min64(k + lookahead, n_local);
-        for (int64_t q = k; q < end; ++q) {
+        // loads issued but not consumed: items k .. issued - 1
+        for (int64_t q = k; q < issued; ++q) {
             const int st = (int)(q % stages);
             ptx::mbar_wait(full0 + 8u * st, (uint32_t)((q / stages) & 1), kDrainLimitNs);
         }
@@ -309,8 +408,8 @@ __global__ void __launch_bounds__(kAgWarps * 32)
         tma_prefetch(&out.map[threadIdx.x]);
     __syncthreads();
 
-    const Walk walk = make_walk(a, warp, npipe);
-    const int64_t first = walk.first, step = walk.step, n_local = walk.n;
+    int dest;
+    Feed feed = make_feed(a, warp, npipe, lane, &dest);
     const int lookahead = stages - D;
     const uint32_t ring = ptx::smem_addr(smem + kAgHeader) + (uint32_t)(warp * stages * stage_bytes);
     const uint32_t full0 = ptx::smem_addr(&sh.full[warp][0]);
@@ -318,31 +417,42 @@ __global__ void __launch_bounds__(kAgWarps * 32)
     const int bn = (int)(a.bn_b / a.es);
     const int grp = (a.dests_per_wait > 0 && a.dests_per_wait < a.W) ? a.dests_per_wait : a.W;
 
-    auto issue_load = [&](int64_t k) {
-        const Item it = decode_item(a, first + k * step);
-        const int st = (int)(k % stages);
-        const uint32_t bar = full0 + 8u * st;
-        if (a.inject_stall && k == 0 && blockIdx.x == 0 && warp == 0)
-            return;  // test hook: this stage's barrier phase never completes
+    int64_t issued = 0;
+    auto issue_next = [&]() {
+        const int64_t t = feed_next(feed, lane);
+        if (t < 0)
+            return;
+        if (issued >= stages) {
+            ptx::bulk_wait_read<D>();
+            __syncwarp();
+        }
+        const int st = (int)(issued % stages);
+        const bool stall = a.inject_stall && issued == 0 && blockIdx.x == 0 && warp == 0;
+        ++issued;
         if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(bar, box_bytes);
-            const int h = a.in_abs ? 0 : a.rank_start + it.g * a.rank_stride;
-            const uint32_t dst = ring + (uint32_t)st * stage_bytes;
-            if (a.mode == kModeAllToAll)
-                tma_load_box4(dst, &in_map, (int)it.tn * bn, (int)(it.tm * a.bm), it.d, h, bar);
-            else
-                tma_load_box(dst, &in_map, (int)it.tn * bn, (int)(it.tm * a.bm), h, bar);
+            const Item it = decode_item(a, t);
+            sh.item[warp][st] = it;
+            if (!stall) {  // test hook: a stalled stage's barrier phase never completes
+                const uint32_t bar = full0 + 8u * st;
+                ptx::mbar_arrive_expect_tx(bar, box_bytes);
+                const int h = a.in_abs ? 0 : a.rank_start + it.g * a.rank_stride;
+                const uint32_t dst = ring + (uint32_t)st * stage_bytes;
+                if (a.mode == kModeAllToAll)
+                    tma_load_box4(dst, &in_map, (int)it.tn * bn, (int)(it.tm * a.bm), it.d, h,
+                                  bar);
+                else
+                    tma_load_box(dst, &in_map, (int)it.tn * bn, (int)(it.tm * a.bm), h, bar);
+            }
         }
         __syncwarp();
     };
 
-    const int64_t preload = gg_min64(lookahead, n_local);
-    for (int64_t k = 0; k < preload; ++k)
-        issue_load(k);
+    for (int q = 0; q < lookahead; ++q)
+        issue_next();
 
     int64_t k = 0;
     bool ok = true;
-    for (; k < n_local; ++k) {
+    for (; k < issued; ++k) {
         const int st = (int)(k % stages);
         const uint32_t parity = (uint32_t)((k / stages) & 1);
         const bool mine = ptx::mbar_wait(full0 + 8u * st, parity, a.wait_limit_ns);
@@ -350,7 +460,7 @@ __global__ void __launch_bounds__(kAgWarps * 32)
             ok = false;
             break;
         }
-        const Item it = decode_item(a, first + k * step);
+        const Item it = sh.item[warp][st];
         const uint32_t buf = ring + (uint32_t)st * stage_bytes;
         const int c0 = (int)it.tn * bn, c1 = (int)(it.tm * a.bm);
         if (a.mode == kModeGather) {
@@ -373,24 +483,17 @@ __global__ void __launch_bounds__(kAgWarps * 32)
         } else {
             // one destination: the program's own (partitioned) or the block's (all-to-all)
             if (lane == 0)
-                tma_store_box(&out.map[a.mode == kModePartitioned ? walk.dest : it.d], buf, c0, c1,
+                tma_store_box(&out.map[a.mode == kModePartitioned ? dest : it.d], buf, c0, c1,
                               it.g);
             ptx::bulk_commit();
         }
-        const int64_t kk = k + lookahead;
-        if (kk < n_local) {
-            if (kk >= stages) {
-                ptx::bulk_wait_read<D>();
-                __syncwarp();
-            }
-            issue_load(kk);
-        }
+        __syncwarp();
+        issue_next();
     }
 
     if (!ok) {
         report_status(a.status, kStatusTimeout);
-        const int64_t end = gg_min64(k + lookahead, n_local);
-        for (int64_t q = k; q < end; ++q) {
+        for (int64_t q = k; q < issued; ++q) {
             const int st = (int)(q % stages);
             ptx::mbar_wait(full0 + 8u * st, (uint32_t)((q / stages) & 1), kDrainLimitNs);
         }
@@ -496,6 +599,46 @@ bool ring_geometry(int64_t stage_raw, int programs, int target, int *npipe, int 
     return false;
 }
 
+// Claimed runs (GatherArgs::work) on the tensor-map path for the all-gather
+// and the all-to-all: about 64 runs per pipeline, 2 to 8 items a run; the
+// counter is zeroed on the launch's stream first (one memset of a few
+// microseconds).  Automatic choice: only launches that move at least
+// kClaimAutoBytes over at least 3/4 of the SMs claim.  Below that every SM
+// gets the bandwidth it asks for, and claims only add their per-run cost
+// (measured on GB300: 5-7% slower at 16-64 programs, 8-16% faster at 128-148
+// programs for the larger all-gathers); the bulk path and the partitioned
+// all-gather lost 5-7% with claims even at 148 programs and keep fixed shares.
+constexpr int64_t kClaimAutoBytes = 256ll << 20;
+
+static cudaError_t prepare_claims(GatherArgs &a, int programs, int npipe, cudaStream_t s)
+{
+    if (!a.work || a.mode == kModePartitioned || a.claim_policy == kClaimNever) {
+        a.work = nullptr;
+        return cudaSuccess;
+    }
+    const int64_t pipes = (int64_t)programs * npipe;
+    const int64_t stores = a.mode == kModeGather ? a.W : 1;  // per item loaded
+    const int64_t bytes = a.total_items * a.bm * a.bn_b * (1 + stores);
+    int64_t c = a.total_items / (pipes * 64);
+    c = c < 2 ? 2 : (c > 8 ? 8 : c);
+    bool claim = a.total_items >= 4 * pipes * c;
+    if (claim && a.claim_policy == kClaimAuto) {
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        claim = bytes >= kClaimAutoBytes && 4 * (int64_t)programs >= 3 * (int64_t)sms;
+    }
+    if (!claim) {
+        a.work = nullptr;
+        return cudaSuccess;
+    }
+    a.chunk = (int)c;
+    return cudaMemsetAsync(a.work, 0, sizeof(unsigned long long), s);
+}
+
 template <int D>
 static cudaError_t launch_bulk_depth(const GatherArgs &a, int programs, int npipe, int stages,
                                      int stage_bytes, cudaStream_t s)
@@ -523,14 +666,18 @@ static cudaError_t launch_tma_depth(const CUtensorMap &in_map, const OutMaps &ou
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather_tma(const CUtensorMap &in_map, const OutMaps &out, const GatherArgs &a,
+cudaError_t launch_gather_tma(const CUtensorMap &in_map, const OutMaps &out, const GatherArgs &args,
                               int programs, cudaStream_t s)
 {
+    GatherArgs a = args;
     int npipe, stages, depth, stage_bytes;
     const int target = a.mode == kModeGather ? kAgTargetPipes : kAgTargetPipesSingle;
     if (!ring_geometry((int64_t)a.bm * a.bn_b, programs, target, &npipe, &stages, &depth,
                        &stage_bytes))
         return cudaErrorInvalidValue;
+    cudaError_t e = prepare_claims(a, programs, npipe, s);
+    if (e != cudaSuccess)
+        return e;
     switch (depth) {
     case 4: return launch_tma_depth<4>(in_map, out, a, programs, npipe, stages, stage_bytes, s);
     case 2: return launch_tma_depth<2>(in_map, out, a, programs, npipe, stages, stage_bytes, s);
@@ -538,12 +685,14 @@ cudaError_t launch_gather_tma(const CUtensorMap &in_map, const OutMaps &out, con
     }
 }
 
-cudaError_t launch_gather_bulk(const GatherArgs &a, int programs, cudaStream_t s)
+cudaError_t launch_gather_bulk(const GatherArgs &args, int programs, cudaStream_t s)
 {
+    GatherArgs a = args;
     int npipe, stages, depth, stage_bytes;
     if (!ring_geometry((int64_t)a.bm * a.bn_b, programs, kAgTargetPipes, &npipe, &stages, &depth,
                        &stage_bytes))
         return cudaErrorInvalidValue;  // tile too large (the host validates first)
+    a.work = nullptr;  // fixed shares (claims do not pay off on this path)
     switch (depth) {
     case 4: return launch_bulk_depth<4>(a, programs, npipe, stages, stage_bytes, s);
     case 2: return launch_bulk_depth<2>(a, programs, npipe, stages, stage_bytes, s);

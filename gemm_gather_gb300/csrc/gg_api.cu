@@ -18,13 +18,30 @@ struct gg_heap {
     int H;
     uint64_t *dev_table;
     std::vector<uint64_t> host_bases;
+    unsigned long long *work = nullptr;  // workspace slots (claimed-run counters)
+    int work_slots = 0;
+    mutable std::atomic<uint32_t> work_next{0};  // round-robin slot of the next launch
+
+    unsigned long long *next_work_slot() const
+    {
+        if (!work)
+            return nullptr;
+        const uint32_t s = work_next.fetch_add(1, std::memory_order_relaxed) % (uint32_t)work_slots;
+        return work + (size_t)s * (GG_WORKSPACE_SLOT_BYTES / sizeof(unsigned long long));
+    }
 };
+
+static_assert(GG_WORKSPACE_SLOT_BYTES == gg::kWorkSlotBytes, "one counter per workspace slot");
+static_assert(GG_CLAIM_AUTO == gg::kClaimAuto && GG_CLAIM_ALWAYS == gg::kClaimAlways &&
+                  GG_CLAIM_NEVER == gg::kClaimNever,
+              "claim policies");
 
 namespace {
 
 thread_local std::string g_last_error;
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_inject_stall{0};
+std::atomic<int> g_claim_policy{GG_CLAIM_AUTO};
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 gg_status fail(gg_status s, const char *fmt, ...)
@@ -198,6 +215,28 @@ gg_status gg_heap_destroy(gg_heap *heap)
     return ok();
 }
 
+gg_status gg_heap_set_workspace(gg_heap *heap, void *dev_work, size_t bytes)
+{
+    if (!heap)
+        return fail(GG_ERR_INVALID_ARG, "heap is NULL");
+    if (!dev_work || bytes == 0) {
+        if (dev_work || bytes)
+            return fail(GG_ERR_INVALID_ARG, "a workspace needs both a pointer and a size");
+        heap->work = nullptr;
+        heap->work_slots = 0;
+        return ok();
+    }
+    if (reinterpret_cast<uint64_t>(dev_work) % 256 != 0)
+        return fail(GG_ERR_ALIGNMENT, "the workspace must be 256-byte aligned");
+    if (bytes % GG_WORKSPACE_SLOT_BYTES != 0 || bytes / GG_WORKSPACE_SLOT_BYTES > (1u << 20))
+        return fail(GG_ERR_INVALID_ARG,
+                    "workspace bytes %zu: a multiple of %d, at most 2^20 slots", bytes,
+                    GG_WORKSPACE_SLOT_BYTES);
+    heap->work = static_cast<unsigned long long *>(dev_work);
+    heap->work_slots = (int)(bytes / GG_WORKSPACE_SLOT_BYTES);
+    return ok();
+}
+
 }  // extern "C"
 
 namespace {
@@ -316,6 +355,9 @@ gg_status prepare_gather(const gg_heap *heap, int mode, int rank, const void *in
     a.status = dev_status;
     a.wait_limit_ns = g_wait_limit_ns.load();
     a.inject_stall = g_inject_stall.load();
+    a.work = nullptr;  // a slot is taken at launch time
+    a.chunk = 0;
+    a.claim_policy = g_claim_policy.load();
 
     // widest power-of-two granule dividing every address, pitch and length
     uint64_t g = in_align | (uint64_t)out_off | (uint64_t)a.ld_in_b | (uint64_t)a.ld_out_b |
@@ -406,6 +448,9 @@ gg_status run_collective(const gg_heap *heap, int mode, int rank, const void *in
     if (st != GG_OK || !launch)
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // a workspace slot for launches that may claim runs (see prepare_claims)
+    if (kind == kTma && mode != gg::kModePartitioned && a.claim_policy != GG_CLAIM_NEVER)
+        a.work = heap->next_work_slot();
     cudaError_t e;
     if (kind == kTma)
         e = gg::launch_gather_tma(in_map, maps, a, comm_programs, s);
@@ -668,6 +713,16 @@ gg_status gg_set_wait_limit_ns(uint64_t ns)
 }
 
 uint64_t gg_get_wait_limit_ns(void) { return g_wait_limit_ns.load(); }
+
+gg_status gg_set_claim_policy(int policy)
+{
+    if (policy != GG_CLAIM_AUTO && policy != GG_CLAIM_ALWAYS && policy != GG_CLAIM_NEVER)
+        return fail(GG_ERR_INVALID_ARG, "unknown claim policy %d", policy);
+    g_claim_policy.store(policy);
+    return ok();
+}
+
+int gg_get_claim_policy(void) { return g_claim_policy.load(); }
 
 gg_status gg_debug_inject_stall(int enable)
 {

@@ -56,7 +56,17 @@ struct GatherArgs {
     int *status;
     uint64_t wait_limit_ns;
     int inject_stall;  // test hook: program 0 never arms its first stage
+    // Claimed-run counter (tensor-map path), set to zero before the launch
+    // when runs are claimed; null: every pipeline walks a fixed share of the
+    // items.
+    unsigned long long *work;
+    int chunk;         // items per claimed run
+    int claim_policy;  // kClaimAuto / kClaimAlways / kClaimNever
 };
+
+constexpr int kClaimAuto = 0, kClaimAlways = 1, kClaimNever = 2;
+// Bytes of one workspace slot (a counter, padded to its own 128 bytes).
+constexpr int kWorkSlotBytes = 128;
 
 // Bulk path: 16-byte aligned addresses, pitches, bn_b and row_b.
 cudaError_t launch_gather_bulk(const GatherArgs &a, int programs, cudaStream_t s);

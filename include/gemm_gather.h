@@ -106,6 +106,44 @@ gg_status gg_heap_info(const gg_heap *heap, int *num_heaps, size_t *bytes_per_ra
 gg_status gg_heap_destroy(gg_heap *heap);
 
 /* ---------------------------------------------------------------------------
+ * gg_heap_set_workspace — give the all-gather and all-to-all launches on
+ * `heap` a workspace of `bytes` bytes of device memory (caller-owned,
+ * 256-byte aligned, a positive multiple of GG_WORKSPACE_SLOT_BYTES, at most
+ * 2^20 slots) for load balancing; NULL with bytes == 0 removes it.  The pages
+ * have no counterpart: their programs each walk a fixed share of the tiles.
+ *
+ * With a workspace, a tensor-map-path launch that the claim policy (below)
+ * selects hands tiles out in short runs claimed from a counter, instead of a
+ * fixed share per program: programs on SMs that get more memory bandwidth
+ * claim more runs, so all of them finish together.  Results are identical.
+ * Such a launch takes the next slot of the workspace (round robin) and zeroes
+ * its counter on its own stream before the kernel (one memset).  Launches on
+ * one heap that may run at the same time (different streams, not ordered)
+ * must number at most bytes / GG_WORKSPACE_SLOT_BYTES: two running launches
+ * that share a slot may skip or repeat tiles (no access outside their
+ * buffers and no hang, but wrong results).  This call touches no device
+ * memory; the workspace must stay allocated while launches use it.
+ * ------------------------------------------------------------------------- */
+#define GG_WORKSPACE_SLOT_BYTES 128
+gg_status gg_heap_set_workspace(gg_heap *heap, void *dev_work, size_t bytes);
+
+/* Which launches claim runs (given a workspace):
+ *   GG_CLAIM_AUTO (default): tensor-map all-gathers and all-to-alls that move
+ *     at least 256 MiB of tile bytes (read plus written) with comm_programs at
+ *     least 3/4 of the device's SMs, where the SMs compete for bandwidth;
+ *   GG_CLAIM_ALWAYS: every tensor-map all-gather and all-to-all with at least
+ *     a few runs per pipeline;
+ *   GG_CLAIM_NEVER: fixed shares only.
+ * The bulk and vector paths and the partitioned all-gather always keep fixed
+ * shares.  Applies to launches made after the call, from any thread;
+ * GG_ERR_INVALID_ARG for another value. */
+#define GG_CLAIM_AUTO 0
+#define GG_CLAIM_ALWAYS 1
+#define GG_CLAIM_NEVER 2
+gg_status gg_set_claim_policy(int policy);
+int gg_get_claim_policy(void);
+
+/* ---------------------------------------------------------------------------
  * gg_all_gather — the persistent tiled all-gather (iris PR #626, "Triton CCL
  * all-gather"; iris #594, "PR description"; iris #591, Description §1).
  *

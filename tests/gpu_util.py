@@ -7,10 +7,11 @@ import numpy as np
 import torch
 
 
-def device_heap(lay, host: np.ndarray):
-    """A SymmetricHeap with the same partitions as ``lay`` holding ``host``."""
+def device_heap(lay, host: np.ndarray, workspace_slots: int = 64):
+    """A SymmetricHeap with the same partitions as ``lay`` holding ``host``
+    (``workspace_slots`` 0: no load-balancing workspace, fixed shares)."""
     import gemm_gather_gb300 as gg
-    sh = gg.SymmetricHeap(lay.H, lay.part_bytes, device="cuda")
+    sh = gg.SymmetricHeap(lay.H, lay.part_bytes, device="cuda", workspace_slots=workspace_slots)
     assert sh.part_bytes == lay.part_bytes
     sh.storage.copy_(torch.from_numpy(host).to("cuda"))
     return sh

@@ -60,6 +60,41 @@ def test_heap_wrap_rejects(args, status):
     assert e.value.status == status
 
 
+def test_heap_workspace_accepts_and_clears(heap):
+    slot = _lib.GG_WORKSPACE_SLOT_BYTES
+    gg.heap_set_workspace(heap, BASE + (1 << 30), 64 * slot)
+    gg.heap_set_workspace(heap, BASE + (1 << 30), slot)
+    gg.heap_set_workspace(heap, None, 0)          # removed: fixed shares again
+    assert ag(heap) == "tma"                      # validation is unaffected
+
+
+@pytest.mark.parametrize("ptr,nbytes,status", [
+    (BASE + 128, 512, _lib.GG_ERR_ALIGNMENT),     # not 256-byte aligned
+    (BASE, 500, _lib.GG_ERR_INVALID_ARG),         # not whole slots
+    (BASE, 0, _lib.GG_ERR_INVALID_ARG),           # pointer without a size
+    (None, 512, _lib.GG_ERR_INVALID_ARG),         # size without a pointer
+    (BASE, 512 * ((1 << 20) + 1), _lib.GG_ERR_INVALID_ARG),  # too many slots
+])
+def test_heap_workspace_rejects(heap, ptr, nbytes, status):
+    with pytest.raises(gg.GGError) as e:
+        gg.heap_set_workspace(heap, ptr, nbytes)
+    assert e.value.status == status
+
+
+def test_claim_policy_round_trip():
+    assert gg.get_claim_policy() == "auto"
+    for p in ("always", "never", "auto"):
+        gg.set_claim_policy(p)
+        assert gg.get_claim_policy() == p
+    for bad in (-1, 3):
+        assert _lib.lib.gg_set_claim_policy(bad) == _lib.GG_ERR_INVALID_ARG
+    assert gg.get_claim_policy() == "auto"
+
+
+def test_heap_workspace_needs_a_heap():
+    assert _lib.lib.gg_heap_set_workspace(None, BASE, 512) == _lib.GG_ERR_INVALID_ARG
+
+
 def ag(heap, **kw):
     a = dict(rank=-1, input=BASE + 4096, ld_in=256, output=BASE + (1 << 20), ld_out=256, M=64,
              N=256, dtype=torch.float16, tile=(8, 256), comm_programs=4, group=(0, 1, 2),

@@ -85,6 +85,10 @@ def test_gather_full_size(oracle, case):
                   tile, programs, group, status=status, path=path)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+    # the automatic claim policy: tensor maps over >= 3/4 of the SMs claim runs
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    claimed = int(sh.workspace.view(torch.int64)[0].item()) > 0
+    assert claimed == (path == "auto" and 4 * programs >= 3 * sms), claimed
     # every byte: block i of every member == member i's input
     for d in members:
         out = sh.view(d, out_off, W * M, N, N, dtype)

@@ -1,9 +1,11 @@
 """CUDA graphs and randomized parity.
 
-* The public calls enqueue only kernel launches on the caller's stream (the
-  host does its validation and tensor-map encoding before the launch), so a
-  whole step -- gather + fused -- can be captured into a CUDA graph and
-  replayed; the replay must give the oracle's heap.
+* The public calls enqueue only kernel launches on the caller's stream (and,
+  for a launch that claims runs of tiles, one memset of its workspace
+  counter); the host does its validation and tensor-map encoding before the
+  launch.  So a whole step -- gather + fused -- can be captured into a CUDA
+  graph and replayed; the replay must give the oracle's heap, with fixed
+  shares and with claimed runs (the memset is replayed with the kernel).
 * Seeded random configurations of the gather, the partitioned gather and the
   all-to-all (group, shape, tile, pitches, programs, path, dtype) must match
   the oracle over the whole heap.
@@ -19,9 +21,10 @@ from tests.gpu_util import device_heap, download, first_diff
 pytestmark = pytest.mark.gpu
 
 
-def test_step_captured_in_a_cuda_graph(oracle):
+@pytest.mark.parametrize("policy,M,N,programs", [("auto", 48, 512, 16), ("always", 256, 1024, 2)])
+def test_step_captured_in_a_cuda_graph(oracle, policy, M, N, programs):
     import gemm_gather_gb300 as gg
-    W, M, N = 4, 48, 512
+    W = 4
     Mf, Nf, Kf = 256, 512, 192
     es = 2
     # one heap holding the gather's and the fused call's buffers
@@ -47,24 +50,31 @@ def test_step_captured_in_a_cuda_graph(oracle):
 
     def step():
         gg.all_gather(sh.heap, -1, sh.ptr(0, in_off), N, sh.ptr(0, out_off), N, M, N,
-                      torch.float16, (8, 256), 16, (0, 1, W), status=status, stream=stream)
+                      torch.float16, (8, 256), programs, (0, 1, W), status=status, stream=stream)
         gg.matmul_all_gather(sh.heap, -1, sh.ptr(0, a_off), Kf, Bd, Nf, sh.ptr(0, c_off), Nf,
                              Mf, Nf, Kf, torch.float16, gg.FUSED_TILE, 8, (0, 1, W),
                              status=status, stream=stream)
 
-    # warm once outside the graph (first-use set-up), then capture and replay
-    with torch.cuda.stream(stream):
-        step()
-    torch.cuda.synchronize()
-    sh.storage.copy_(torch.from_numpy(host).cuda())
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        step()
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
+    gg.set_claim_policy(policy)
+    try:
+        # warm once outside the graph (first-use set-up), then capture and replay
+        with torch.cuda.stream(stream):
+            step()
+        torch.cuda.synchronize()
+        sh.storage.copy_(torch.from_numpy(host).cuda())
+        sh.workspace.zero_()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+    finally:
+        gg.set_claim_policy("auto")
     assert int(status.item()) == 0
+    # the captured gather used workspace slot 1 (the warm-up took slot 0)
+    assert (int(sh.workspace.view(torch.int64)[16].item()) > 0) == (policy == "always")
     got = download(sh)
     oracle.all_gather(host, part, in_off, N, out_off, N, M, N, es, (0, 1, W))
     oracle.matmul_all_gather(host, part, a_off, Kf, B.view(torch.int16).numpy().view(np.uint16),
