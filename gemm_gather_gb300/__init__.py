@@ -24,7 +24,7 @@ from ._lib import (GG_AG_AUTO, GG_AG_BULK, GG_AG_TMA, GG_AG_VECTOR, GG_BF16, GG_
 
 __all__ = [
     "heap_create", "heap_wrap", "heap_bases", "heap_info", "heap_destroy", "heap_set_workspace",
-    "all_gather",
+    "all_gather", "all_gather_noalloc",
     "all_gather_check", "all_gather_grouped", "all_gather_partitioned", "all_to_all",
     "collective_check", "matmul_all_gather", "matmul_all_gather_check", "set_claim_policy",
     "get_claim_policy", "CLAIM_POLICIES", "set_wait_limit_ns",
@@ -124,6 +124,17 @@ def all_gather(heap: Heap, rank: int, input, ld_in: int, output, ld_out: int, M:
     check(lib.gg_all_gather_path(heap.handle, rank, _ptr(input), ld_in, _ptr(output), ld_out, M,
                                  N, _dtype(dtype), Tile(*tile), comm_programs, Group(*group),
                                  _ptr(status), _stream(stream), PATHS[path]))
+
+
+def all_gather_noalloc(heap: Heap, rank: int, input, ld_in: int, output, ld_out: int, M: int,
+                       N: int, dtype, tile: tuple[int, int], comm_programs: int,
+                       group: tuple[int, int, int], status=None, stream=None) -> None:
+    """gg_all_gather for callers that cannot allocate device memory: a
+    claiming launch keeps its counter in the library's static device array
+    (shared by every call on the device; calls that overlap on the GPU race)."""
+    check(lib.gg_all_gather_noalloc(heap.handle, rank, _ptr(input), ld_in, _ptr(output), ld_out,
+                                    M, N, _dtype(dtype), Tile(*tile), comm_programs, Group(*group),
+                                    _ptr(status), _stream(stream)))
 
 
 def all_gather_check(heap: Heap, rank: int, input, ld_in: int, output, ld_out: int, M: int,

@@ -33,7 +33,8 @@ GG_CLAIM_AUTO, GG_CLAIM_ALWAYS, GG_CLAIM_NEVER = 0, 1, 2
 EXPORTS = (
     "gg_heap_create", "gg_heap_wrap", "gg_heap_bases", "gg_heap_info", "gg_heap_destroy",
     "gg_heap_set_workspace",
-    "gg_all_gather", "gg_all_gather_path", "gg_all_gather_check", "gg_all_gather_grouped",
+    "gg_all_gather", "gg_all_gather_noalloc", "gg_all_gather_path", "gg_all_gather_check",
+    "gg_all_gather_grouped",
     "gg_all_gather_partitioned", "gg_all_to_all", "gg_collective_check",
     "gg_matmul_all_gather", "gg_matmul_all_gather_path", "gg_matmul_all_gather_check",
     "gg_set_claim_policy", "gg_get_claim_policy",
@@ -64,6 +65,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "gg_heap_set_workspace": ([vp, vp, sz], i32),
         "gg_all_gather": ([vp, i32, vp, i64, vp, i64, i64, i64, i32, Tile, i32, Group, vp, vp],
                           i32),
+        "gg_all_gather_noalloc": ([vp, i32, vp, i64, vp, i64, i64, i64, i32, Tile, i32, Group, vp,
+                                   vp], i32),
         "gg_all_gather_path": ([vp, i32, vp, i64, vp, i64, i64, i64, i32, Tile, i32, Group, vp,
                                 vp, i32], i32),
         "gg_all_gather_check": ([vp, i32, vp, i64, vp, i64, i64, i64, i32, Tile, i32, Group, i32,

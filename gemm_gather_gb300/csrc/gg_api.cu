@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -747,5 +748,92 @@ const char *gg_status_string(gg_status s)
 }
 
 int gg_version(void) { return 100; }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free all-gather (gg_all_gather_noalloc).
+//
+// For callers that cannot allocate device memory at all (no cudaMalloc, no
+// allocator of their own to carve a workspace from), the claim counter of the
+// load-balanced tensor-map path lives in this file-scope device array instead
+// of a heap workspace.  It is a single region shared by every call on a
+// device, and holds the last call's counter until the next claiming call
+// zeroes it (one memset on that call's stream).  Every GPU that loads the
+// library keeps these bytes until the process exits.
+// ---------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = 256;
+static __device__ __align__(256) unsigned long long g_noalloc_scratch[kNoAllocScratchBytes / 8];
+static_assert(sizeof(unsigned long long) <= kNoAllocScratchBytes,
+              "a call needs one claim counter, whatever its sizes");
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+unsigned long long *g_noalloc_dev_ptr[kNoAllocMaxDevices];
+
+// Device address of the scratch array on the current device: looked up once
+// per device (with that device current), then cached.
+gg_status noalloc_scratch(unsigned long long **out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kNoAllocMaxDevices)
+        return fail(GG_ERR_UNSUPPORTED, "device %d: the allocation-free call serves devices 0..%d",
+                    dev, kNoAllocMaxDevices - 1);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_dev_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress of the static scratch array");
+        g_noalloc_dev_ptr[dev] = static_cast<unsigned long long *>(p);
+    }
+    *out = g_noalloc_dev_ptr[dev];
+    return GG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gg_status gg_all_gather_noalloc(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
+                                void *output, int64_t ld_out, int64_t M, int64_t N,
+                                gg_dtype dtype, gg_tile tile, int comm_programs, gg_group group,
+                                int *dev_status, gg_stream_t stream)
+{
+    unsigned long long *scratch = nullptr;
+    gg_status st = noalloc_scratch(&scratch);  // first call on a device: set-up
+    if (st != GG_OK)
+        return st;
+    gg::GatherArgs a;
+    int kind = kVector, vec = 0;
+    bool launch = false;
+    static thread_local CUtensorMap in_map;
+    static thread_local gg::OutMaps maps;
+    st = prepare_gather(heap, gg::kModeGather, rank, input, ld_in, output, ld_out, M, N, dtype,
+                        tile, comm_programs, group, 0, dev_status, GG_AG_AUTO, &a, &kind, &vec,
+                        &in_map, &maps, &launch);
+    if (st != GG_OK || !launch)
+        return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // the static counter stands in for a heap workspace slot; the launch
+    // zeroes it on `s` when it claims runs
+    if (kind == kTma && a.claim_policy != GG_CLAIM_NEVER)
+        a.work = scratch;
+    cudaError_t e;
+    if (kind == kTma)
+        e = gg::launch_gather_tma(in_map, maps, a, comm_programs, s);
+    else if (kind == kBulk)
+        e = gg::launch_gather_bulk(a, comm_programs, s);
+    else
+        e = gg::launch_gather_vec(a, comm_programs, vec, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "launching the allocation-free all-gather");
+    return ok();
+}
 
 }  // extern "C"

@@ -176,6 +176,36 @@ gg_status gg_all_gather(const gg_heap *heap, int rank, const void *input, int64_
                         gg_tile tile, int comm_programs, gg_group group, int *dev_status,
                         gg_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * gg_all_gather_noalloc — gg_all_gather for callers that cannot allocate
+ * device memory.  The pages have no counterpart (they allocate freely).
+ *
+ * Who needs it: code that may not call cudaMalloc, or any allocator, once it
+ * is running -- a plugin inside a framework that owns all device memory, a
+ * real-time loop where an allocation's implicit device synchronization is not
+ * allowed, a process whose memory budget is fixed at start-up -- and that
+ * therefore has no device buffer to hand gg_heap_set_workspace.
+ *
+ * Same arguments, validation and results as gg_all_gather (automatic data
+ * path, claim policy of gg_set_claim_policy; the heap's workspace, if any, is
+ * not used).  When the launch claims runs of tiles, its counter lives in a
+ * 256-byte static device array inside this library instead of a workspace;
+ * the call zeroes that counter with one memset on `stream` before the kernel
+ * and allocates nothing.  The scratch needed does not grow with M, N,
+ * world_size or comm_programs (one 8-byte counter), so no size the all-gather
+ * accepts is rejected for lack of scratch.
+ * Limits: every GPU that loads the library holds the 256 bytes until the
+ * process exits; all calls on a device share the one counter, so calls that
+ * may overlap on the GPU (different streams, not ordered) race and may skip
+ * or repeat tiles -- order them on one stream.  The first call on each device
+ * (with that device current) looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * ------------------------------------------------------------------------- */
+gg_status gg_all_gather_noalloc(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
+                                void *output, int64_t ld_out, int64_t M, int64_t N,
+                                gg_dtype dtype, gg_tile tile, int comm_programs, gg_group group,
+                                int *dev_status, gg_stream_t stream);
+
 /* Data-path variants of gg_all_gather (same arguments and result):
  *   GG_AG_AUTO      tensor-map path when it applies, else bulk, else vector
  *                   (what gg_all_gather does)
