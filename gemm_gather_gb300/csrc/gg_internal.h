@@ -98,6 +98,8 @@ struct FusedArgs {
     int *status;
     uint64_t wait_limit_ns;
     int inject_stall;  // test hook: CTA 0 never arms its first ring stage
+    int b_boxes3d;     // set by the launcher: B stages load as one 3-d box
+    int tn_group;      // set by the launcher: tile columns per group of the tile order
 };
 
 // variant: 0 = automatic (2-SM pairs when programs >= 2), 1 = 1-SM, 2 = 2-SM

@@ -40,6 +40,13 @@ namespace gg {
 namespace {
 
 constexpr int BM = 128, BN = 256, UK = 16;
+constexpr int kMaxStages = 8;
+// B stages load as one 3-d box (when N is a multiple of 64) instead of one
+// 2-d box per 64 columns: one TMA instruction fewer per stage (measured
+// +0-2.5%).
+constexpr bool kBBoxes3d = true;
+// Bytes of B one column group of the tile order may span (see tile_coord).
+constexpr int64_t kBGroupBytes = 32ll << 20;
 constexpr int kKAtom = 64;                      // K elements of one 128-byte swizzle row
 constexpr int kAAtom = BM * kKAtom * 2;         // 16 KB: 128 rows x 64 K, K-major
 constexpr int kThreads = 192;                   // 6 warps
@@ -81,8 +88,8 @@ struct Geo {
 };
 
 struct FusedShared {
-    uint64_t full[6];
-    uint64_t empty[6];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t mma_done;
@@ -96,6 +103,9 @@ constexpr int smem_bytes()
 {
     return Geo<CG>::kOffShared + (int)sizeof(FusedShared) + 1024;  // + alignment slack
 }
+static_assert(Geo<1>::kStages <= kMaxStages && Geo<2>::kStages <= kMaxStages, "ring barriers");
+static_assert(smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448,
+              "at most 227 KB of dynamic shared memory per CTA");
 
 // ---- tcgen05 / TMA / cluster wrappers --------------------------------------------
 template <int CG>
@@ -413,17 +423,26 @@ struct TileCoord {
     int tm, tn;
 };
 
+// Tile order: the tile columns are split into groups of a.tn_group; group by
+// group, every (source, tile row) runs over the group's columns.  A group's
+// slice of B stays in L2 while the tile rows stream past it (B would
+// otherwise be re-read from DRAM once per wave of tiles); A is read once per
+// group.
 __device__ __forceinline__ TileCoord tile_coord(const FusedArgs &a, int64_t t, int tiles_m,
                                                 int tiles_n)
 {
     TileCoord c;
-    const int64_t per_src = (int64_t)tiles_m * tiles_n;
-    const int s = (int)(t / per_src);
-    const int64_t rem = t - (int64_t)s * per_src;
+    const int gw = a.tn_group;
+    const int64_t rows = (int64_t)a.n_src * tiles_m;  // (source, tile row) pairs
+    const int j = (int)(t / (rows * gw));              // column group
+    const int64_t r = t - (int64_t)j * rows * gw;
+    const int width = tiles_n - j * gw < gw ? tiles_n - j * gw : gw;
+    const int64_t sr = r / width;
+    const int s = (int)(sr / tiles_m);
     c.g = a.src_first + s;
     c.h = a.rank_start + c.g * a.rank_stride;
-    c.tm = (int)(rem / tiles_n);
-    c.tn = (int)(rem - (int64_t)c.tm * tiles_n);
+    c.tm = (int)(sr - (int64_t)s * tiles_m);
+    c.tn = j * gw + (int)(r - sr * width);
     return c;
 }
 
@@ -523,10 +542,16 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
                     for (int ka = 0; ka < G::kBK / kKAtom; ++ka)
                         tma_load_3d<CG>(sa + ka * kAAtom, &map_a, kq * G::kBK + ka * kKAtom, row0,
                                         h_coord, bar, pol_a);
+                    if (a.b_boxes3d) {
+                        // B viewed as {64 columns, K, N/64 chunks}: the kBCols/64
+                        // boxes of the stage in one copy (same shared layout)
+                        tma_load_3d<CG>(sb, &map_b, 0, kq * G::kBK, col0 / 64, bar, pol_b);
+                    } else {
 #pragma unroll
-                    for (int j = 0; j < G::kBCols / 64; ++j)
-                        tma_load_2d<CG>(sb + j * G::kBBox, &map_b, col0 + j * 64, kq * G::kBK, bar,
-                                        pol_b);
+                        for (int j = 0; j < G::kBCols / 64; ++j)
+                            tma_load_2d<CG>(sb + j * G::kBBox, &map_b, col0 + j * 64, kq * G::kBK,
+                                            bar, pol_b);
+                    }
                 }
                 __syncwarp();
                 ++issued;
@@ -805,7 +830,30 @@ cudaError_t launch_matmul_all_gather(const FusedArgs &a, const OutMaps &out, int
     }
     const bool two_sm = variant != 1 && programs >= 2;
     const int bk = two_sm ? Geo<2>::kBK : Geo<1>::kBK;  // K rows of one B box
+    FusedArgs args = a;
+    args.b_boxes3d = 0;
     {
+        // column groups whose B slice (K x 256 columns each) fits in
+        // kBGroupBytes, as equal as possible
+        const int64_t tn = a.N > BN ? (a.N + BN - 1) / BN : 1;
+        const int64_t per_col = a.K * BN * 2;
+        int64_t w = kBGroupBytes / (per_col > 0 ? per_col : 1);
+        w = w < 1 ? 1 : (w > tn ? tn : w);
+        const int64_t groups = (tn + w - 1) / w;
+        args.tn_group = (int)((tn + groups - 1) / groups);
+    }
+    if (kBBoxes3d && a.N % 64 == 0) {
+        // {64 columns, K, N/64 column chunks}: one copy per stage brings all the
+        // CTA's 64-column boxes (only when N is whole chunks, so no box reads
+        // past the end of a row of B)
+        const uint64_t dims[3] = {64, (uint64_t)a.K, (uint64_t)(a.N / 64)};
+        const uint64_t strides[2] = {(uint64_t)a.ldb * 2, 128};
+        const uint32_t box[3] = {64, (uint32_t)bk,
+                                 (uint32_t)(two_sm ? Geo<2>::kBCols / 64 : Geo<1>::kBCols / 64)};
+        args.b_boxes3d =
+            encode_map(&map_b, dt, 3, a.b, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ? 1 : 0;
+    }
+    if (!args.b_boxes3d) {
         const uint64_t dims[2] = {(uint64_t)a.N, (uint64_t)a.K};
         const uint64_t strides[1] = {(uint64_t)a.ldb * 2};
         const uint32_t box[2] = {64, (uint32_t)bk};
@@ -854,7 +902,7 @@ cudaError_t launch_matmul_all_gather(const FusedArgs &a, const OutMaps &out, int
         int64_t clusters = gg_min64(programs / 2, pairs);
         if (resident > 0)
             clusters = gg_min64(clusters, resident);
-        mag2_kernel<<<(int)(2 * clusters), kThreads, smem_bytes<2>(), s>>>(map_a, map_b, out, a);
+        mag2_kernel<<<(int)(2 * clusters), kThreads, smem_bytes<2>(), s>>>(map_a, map_b, out, args);
     } else {
         const int64_t tiles = (int64_t)a.n_src * ((a.M + BM - 1) / BM) * tiles_n;
         e = cudaFuncSetAttribute(mag1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -864,7 +912,7 @@ cudaError_t launch_matmul_all_gather(const FusedArgs &a, const OutMaps &out, int
             return e;
         }
         mag1_kernel<<<(int)gg_min64(programs, tiles), kThreads, smem_bytes<1>(), s>>>(map_a, map_b,
-                                                                                    out, a);
+                                                                                    out, args);
     }
     return cudaGetLastError();
 }
