@@ -19,7 +19,8 @@
 //            heap-bases table once per launch (the translation hoisted out of
 //            every loop; each map views a member's output as {N, M, W} so a
 //            tile is clipped at the end of its row block).  Same pipeline as
-//            the bulk path.
+//            the bulk path; on large launches the tiles are handed out in
+//            runs claimed from a workspace counter (load balancing, see Feed).
 //  * bulk:   tiles are staged in shared memory by the TMA engine
 //            (cp.async.bulk, completion on an mbarrier) and stored with
 //            cp.async.bulk shared->global, one copy per tile row and
