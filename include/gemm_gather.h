@@ -3,8 +3,9 @@
  * the epilogue of a matmul, for one NVIDIA GB300 (sm_103a).
  *
  * C ABI.  Plain pointers and sizes only.  All device memory is owned by the
- * caller; the library never allocates device memory and keeps no state on
- * the device.  Every call that launches work is asynchronous on the caller's
+ * caller; the library never allocates device memory, and its only device
+ * state is the 256-byte static counter of gg_all_gather_noalloc.  Every call
+ * that launches work is asynchronous on the caller's
  * stream.  Errors found on the host are returned before anything is
  * launched; gg_last_error() then describes them.  No call aborts the process.
  *
