@@ -8,7 +8,8 @@
   shares and with claimed runs (the memset is replayed with the kernel).
 * Seeded random configurations of the gather, the partitioned gather and the
   all-to-all (group, shape, tile, pitches, programs, path, dtype) must match
-  the oracle over the whole heap.
+  the oracle over the whole heap, under the automatic claim policy and with
+  claims forced on.
 """
 import numpy as np
 import pytest
@@ -108,8 +109,12 @@ def _random_cases(n, seed):
     return cases
 
 
+@pytest.mark.parametrize("policy", ["auto", "always"])
 @pytest.mark.parametrize("case", _random_cases(40, 2026), ids=lambda c: f"{c[0]}_W{c[2][2]}_{c[3]}x{c[4]}e{c[5]}t{c[6]}p{c[7]}_{c[10]}")
-def test_random_collective_matches_oracle(oracle, case):
+def test_random_collective_matches_oracle(oracle, case, policy):
+    """"always" makes every tensor-map all-gather / all-to-all with a few runs
+    per pipeline claim them, so the claimed-run walk meets random shapes,
+    tiles and budgets too."""
     import gemm_gather_gb300 as gg
     kind, H, group, M, N, es, tile, programs, pi, po, path = case
     W = group[2]
@@ -132,7 +137,11 @@ def test_random_collective_matches_oracle(oracle, case):
             ld_out, M, N, dt, tile, programs, group)
     fn = {"all_gather": gg.all_gather, "partitioned": gg.all_gather_partitioned,
           "all_to_all": gg.all_to_all}[kind]
-    fn(*args, status=status, path=path)
+    gg.set_claim_policy(policy)
+    try:
+        fn(*args, status=status, path=path)
+    finally:
+        gg.set_claim_policy("auto")
     got = download(sh)
     assert int(status.item()) == 0
     if kind == "all_to_all":
