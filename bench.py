@@ -576,18 +576,21 @@ def run_sweep(args):
         if clocks:
             clocks.start()
             steps = max(steps, int(1.0 / max(work, 1e-6)))  # at least ~1 s under load
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(steps):
-            launch()
-        e1.record()
-        torch.cuda.synchronize(dev)
+        runs = []
+        for _ in range(max(1, args.repeats)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                launch()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            runs.append(e0.elapsed_time(e1) / steps)
         clk = clocks.stop() if clocks else None
-        ms = e0.elapsed_time(e1) / steps
+        ms = statistics.median(runs)
         if int(status.item()) != 0:
             raise RuntimeError(f"device status {int(status.item())}")
         rec = {"sweep": args.sweep, "workload": (g or f).describe(), "ms": ms, "steps": steps,
-               "roofline_ms": 1e3 * work, "frac": 1e3 * work / ms}
+               "runs_ms": runs, "roofline_ms": 1e3 * work, "frac": 1e3 * work / ms}
         moved = gather_bytes(g) if g else fused_bytes(f)
         if moved < 2 * L2_BYTES and args.sweep != "small":
             # small enough to be partly L2-resident between back-to-back launches:
@@ -659,6 +662,8 @@ def main():
                     help="time every point of a configuration sweep (one JSON line each)")
     ap.add_argument("--only", default="", help="sweep: run only points whose description "
                     "contains one of these '|'-separated substrings")
+    ap.add_argument("--repeats", type=int, default=3,
+                    help="sweep: timed runs per point; the median is reported")
     ap.add_argument("--sweep-clocks", action="store_true",
                     help="sample SM clocks while each sweep point runs (about 1 s per point)")
     ap.add_argument("--claims", default=None, choices=["auto", "always", "never"],
