@@ -592,7 +592,6 @@ gg_status prepare_fused(const gg_heap *heap, int rank, const void *A, int64_t ld
         return st;
 
     gg::FusedArgs f{};
-    f.bases = heap->dev_table;
     f.W = W;
     f.rank_start = group.rank_start;
     f.rank_stride = group.rank_stride;

@@ -80,7 +80,6 @@ cudaError_t launch_gather_vec(const GatherArgs &a, int programs, int vec_bytes, 
 // One launch of the fused matmul + all-gather (see mag_kernel.cu).  The
 // outputs are reached through per-member tensor maps (OutMaps).
 struct FusedArgs {
-    const uint64_t *bases;  // device heap-bases table (vector-store epilogue)
     int W, rank_start, rank_stride;
     int n_src, src_first;
     const void *a_abs;     // non-null: the one source's A (any device memory)

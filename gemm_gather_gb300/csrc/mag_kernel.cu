@@ -2,14 +2,20 @@
 // "Benchmark": the matmul's epilogue all-gathers each output tile, with the
 // heap-base translation hoisted above the K loop).
 //
-// C_r = A_r @ B for every source r of the launch, each 128 x 256 output tile:
-//   * warp 0 (producer): TMA tensor loads of A (128 x 64, K-major) and B
-//     (64 x 256, N-major, as four 64-column boxes) into a 3-stage ring of
-//     128B-swizzled shared memory, completion on mbarriers;
-//   * warp 1 (MMA): allocates 512 TMEM columns (two 128 x 256 fp32
-//     accumulators) and issues tcgen05.mma kind::f16 (M=128, N=256, K=16)
-//     from one thread; tcgen05.commit frees ring stages and hands finished
-//     accumulators to the epilogue;
+// C_r = A_r @ B for every source r of the launch.  Persistent CTAs, one per
+// SM; the default kernel (mag2) runs them as CTA pairs (clusters of 2) that
+// compute 256 x 256 tiles with tcgen05.mma.cta_group::2, the 1-SM kernel
+// (mag1) 128 x 256 tiles.  Tiles are taken in column groups whose slice of B
+// stays in L2 (see tile_coord).  Per CTA:
+//   * warp 0 (producer): TMA tensor loads of A (128 x 64, K-major) and of the
+//     CTA's columns of B (64-deep, N-major, 64-column boxes; one 3-d box per
+//     stage when N is a multiple of 64) into a ring of 128B-swizzled stages
+//     (6 on 2 SMs, 4 on 1 SM); a pair's loads complete on the leader's
+//     mbarriers;
+//   * warp 1 (MMA): allocates 512 TMEM columns (two fp32 accumulators) and,
+//     in the leader, issues tcgen05.mma kind::f16 (M=256 or 128, N=256,
+//     K=16) from one thread; tcgen05.commit frees ring stages (in both CTAs
+//     of a pair) and hands finished accumulators to the epilogue;
 //   * warps 2-5 (epilogue): tcgen05.ld of their 32 TMEM lanes (= tile rows),
 //     round to f16/bf16 and write each value once into shared memory as
 //     32-row x 64-column boxes in the 128-byte swizzled layout, then one TMA
@@ -72,13 +78,6 @@ struct Geo {
     // The epilogue stages each warp's 32 rows in column passes of kEpiCols,
     // as kEpiCols/64 swizzled boxes.
     static constexpr int kEpiCols = CG == 1 ? 64 : 128;
-    // Epilogue stores: TMA tensor stores of the staged boxes (false), or
-    // 16-byte vector stores read back from the staged boxes (true).
-    static constexpr bool kEpiVector = false;
-    // Each tile walks its K blocks cyclically from a per-tile starting block,
-    // so tiles sharing an A row block or a B column block do not request the
-    // same slice at the same moment (the f32 accumulation order changes).
-    static constexpr bool kKRotate = false;
     static constexpr int kEpiBoxes = kEpiCols / 64;
     static constexpr int kEpiWarp = kEpiBoxes * kBox;  // one epilogue warp's staging
     static constexpr int kOffA = 0;
@@ -93,7 +92,6 @@ struct FusedShared {
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t mma_done;
-    uint64_t dst[kMaxWorld];  // output base of member i (vector-store epilogue)
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -367,24 +365,6 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi, int bf16)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-
-// Streaming (evict-first) 16-byte global store.
-__device__ __forceinline__ void st_global_cs_v4(void *p, uint4 v)
-{
-    asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d)
 {
@@ -491,12 +471,8 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
         tmem_alloc<CG>(ptx::smem_addr(&sh.tmem_base));
         tc_fence_before();
     }
-    if (threadIdx.x < (unsigned)a.W) {
-        prefetch_tensormap(&out.map[threadIdx.x]);
-        // heap bases -> member output bases, once, before any tile
-        sh.dst[threadIdx.x] =
-            a.bases[a.rank_start + threadIdx.x * a.rank_stride] + (uint64_t)a.out_off;
-    }
+    if (threadIdx.x < (unsigned)a.W)
+        prefetch_tensormap(&out.map[threadIdx.x]);  // the member output maps, once
     __syncthreads();
     if constexpr (CG == 2)
         cluster_sync();  // the peer's barriers exist before anything signals them
@@ -517,12 +493,7 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
             const int h_coord = a.a_abs ? 0 : c.h;
             const int row0 = c.tm * G::kTileM + (int)rank * BM;
             const int col0 = c.tn * BN + (int)rank * G::kBCols;
-            const int k_first =
-                G::kKRotate ? (int)(((int64_t)c.tm * 7 + (int64_t)c.tn * 3 + c.g * 5) % num_kb) : 0;
-            for (int kb = 0; kb < num_kb; ++kb) {
-                int kq = kb + k_first;  // the K block this stage carries
-                if (kq >= num_kb)
-                    kq -= num_kb;
+            for (int kq = 0; kq < num_kb; ++kq) {  // the K block this stage carries
                 const bool got = role_wait(ptx::smem_addr(&sh.empty[stage]), phase ^ 1u,
                                            a.wait_limit_ns, abort_flag);
                 if (!__all_sync(0xffffffffu, got)) {
@@ -716,40 +687,6 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
                 }
                 // staged boxes -> every destination, local first, peers rotated
                 const int col0 = c.tn * BN + pass;
-                if constexpr (G::kEpiVector) {
-                    __syncwarp();  // every row of the boxes is staged
-                    const int64_t ld_out_b = a.ld_out * 2;
-#pragma unroll 1
-                    for (int b = 0; b < G::kEpiBoxes; ++b) {
-                        const int colb = col0 + b * 64;
-                        if (colb >= a.N)
-                            break;
-                        const uint32_t box = warp_stage + (uint32_t)(b * kBox);
-#pragma unroll 2
-                        for (int it = 0; it < 8; ++it) {
-                            // 16-byte chunk: row r of the box, columns 8k..8k+7
-                            const int ch = it * 32 + lane;
-                            const int r = ch >> 3, k = ch & 7;
-                            const uint4 v = ld_shared_v4(box + (uint32_t)(r * 128) +
-                                                         ((uint32_t)(k ^ (r & 7)) << 4));
-                            const int64_t row = (int64_t)row0 + r;
-                            const int col = colb + k * 8;
-                            if (row < a.M && col < a.N) {
-                                const int64_t off = ((int64_t)c.g * a.M + row) * ld_out_b +
-                                                    (int64_t)col * 2;
-                                for (int j = 0; j < a.W; ++j) {
-                                    int i = c.g + j;
-                                    if (i >= a.W)
-                                        i -= a.W;
-                                    st_global_cs_v4(reinterpret_cast<uint8_t *>(sh.dst[i]) + off,
-                                                    v);
-                                }
-                            }
-                        }
-                    }
-                    __syncwarp();  // the boxes may be restaged
-                    continue;
-                }
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (row0 < a.M) {
