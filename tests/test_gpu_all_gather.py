@@ -78,6 +78,9 @@ CASES = [
     (5, (2, 1, 3), 1, 1, 4, (1, 1), 2, 0, 0),                # 1 x 1 blocks
     (8, (0, 1, 8), 100, 4096, 2, (8, 256), 148, 0, 0),       # several waves of work items
     (4, (0, 1, 4), 64, 2048, 4, (256, 32), 3, 0, 0),         # tall tile, few programs
+    (64, (0, 1, 64), 9, 40, 2, (8, 16), 37, 0, 0),           # 64 ranks: stores wrap the lanes
+    (40, (3, 1, 33), 5, 264, 4, (4, 64), 20, 0, 8),          # 33 ranks from heap 3
+    (8, (0, 1, 8), 64, 1024, 2, (8, 256), 400, 0, 0),        # more programs than SMs
 ]
 
 

@@ -41,6 +41,8 @@ PART_CASES = [
     (8, (1, 2, 4), 33, 264, 4, (8, 256), 16, 0, 0),
     (8, (0, 1, 8), 100, 4096, 2, (8, 256), 148, 0, 0),
     (8, (0, 1, 8), 64, 512, 2, (16, 128), 8, 0, 0),        # exactly one program per destination
+    (64, (0, 1, 64), 9, 40, 2, (8, 16), 70, 0, 0),         # 64 destinations
+    (40, (3, 1, 33), 5, 264, 4, (4, 64), 300, 0, 8),       # 33 destinations, more programs than SMs
 ]
 
 
@@ -116,6 +118,8 @@ A2A_CASES = [
     (8, (0, 1, 8), 64, 1024, 2, (8, 256), 148, 0, 0),
     (5, (2, 1, 3), 1, 1, 4, (1, 1), 2, 0, 0),
     (1, (0, 1, 1), 9, 24, 2, (8, 8), 1, 0, 0),
+    (64, (0, 1, 64), 2, 40, 2, (8, 16), 37, 0, 0),         # 64 members
+    (40, (3, 1, 33), 3, 264, 4, (4, 64), 300, 0, 8),       # 33 members, more programs than SMs
 ]
 
 
