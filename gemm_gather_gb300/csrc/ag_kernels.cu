@@ -80,8 +80,9 @@ struct AgShared {
 
 constexpr int kAgHeader = (int)((sizeof(AgShared) + 127) / 128 * 128);
 
-// The items one pipeline (warp) of a program walks: first, first + step, ...
-// and, for the partitioned all-gather, the one destination its program serves.
+// The items a vector-path program walks (the whole program is one pipeline):
+// first, first + step, ... and, for the partitioned all-gather, the one
+// destination it serves.  The ring kernels walk a Feed instead.
 struct Walk {
     int64_t first, step, n;
     int dest;
