@@ -45,6 +45,8 @@
 // previous ones have read shared memory (bulk and tensor-map paths).
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "gg_internal.h"
 #include "ptx.cuh"
 
@@ -641,13 +643,32 @@ static cudaError_t prepare_claims(GatherArgs &a, int programs, int npipe, cudaSt
     return cudaMemsetAsync(a.work, 0, sizeof(unsigned long long), s);
 }
 
+// The ring kernels may use up to kAgSmemBudget bytes of dynamic shared
+// memory: the limit is raised once per device and kernel (a launch then asks
+// for what it uses), not on every launch.
+template <typename Kernel>
+static cudaError_t allow_ring_smem(Kernel kernel, std::atomic<uint64_t> &done_mask)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? 1ull << dev : 0;
+    if (bit && (done_mask.load(std::memory_order_relaxed) & bit))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAgSmemBudget);
+    if (e == cudaSuccess && bit)
+        done_mask.fetch_or(bit, std::memory_order_relaxed);
+    return e;
+}
+
 template <int D>
 static cudaError_t launch_bulk_depth(const GatherArgs &a, int programs, int npipe, int stages,
                                      int stage_bytes, cudaStream_t s)
 {
-    const int smem = kAgHeader + npipe * stages * stage_bytes;
-    cudaError_t e =
-        cudaFuncSetAttribute(ag_bulk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static std::atomic<uint64_t> done{0};
+    const int smem = kAgHeader + npipe * stages * stage_bytes;  // <= kAgSmemBudget
+    cudaError_t e = allow_ring_smem(ag_bulk_kernel<D>, done);
     if (e != cudaSuccess)
         return e;
     ag_bulk_kernel<D><<<programs, npipe * 32, smem, s>>>(a, stages, stage_bytes);
@@ -659,9 +680,9 @@ static cudaError_t launch_tma_depth(const CUtensorMap &in_map, const OutMaps &ou
                                     const GatherArgs &a, int programs, int npipe, int stages,
                                     int stage_bytes, cudaStream_t s)
 {
-    const int smem = kAgHeader + npipe * stages * stage_bytes;
-    cudaError_t e =
-        cudaFuncSetAttribute(ag_tma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static std::atomic<uint64_t> done{0};
+    const int smem = kAgHeader + npipe * stages * stage_bytes;  // <= kAgSmemBudget
+    cudaError_t e = allow_ring_smem(ag_tma_kernel<D>, done);
     if (e != cudaSuccess)
         return e;
     ag_tma_kernel<D><<<programs, npipe * 32, smem, s>>>(in_map, out, a, stages, stage_bytes);
