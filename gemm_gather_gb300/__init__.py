@@ -28,7 +28,8 @@ __all__ = [
     "all_gather_check", "all_gather_grouped", "all_gather_partitioned", "all_to_all",
     "collective_check", "matmul_all_gather", "matmul_all_gather_check", "set_claim_policy",
     "get_claim_policy", "CLAIM_POLICIES", "set_wait_limit_ns",
-    "get_wait_limit_ns", "debug_inject_stall", "SymmetricHeap", "Heap", "GGError", "DTYPE_CODES", "PATHS",
+    "get_wait_limit_ns", "debug_inject_stall", "device_status", "clear_device_status",
+    "SymmetricHeap", "Heap", "GGError", "DTYPE_CODES", "PATHS",
     "FUSED_TILE", "FUSED_PATHS",
 ]
 
@@ -234,6 +235,19 @@ def get_wait_limit_ns() -> int:
 
 def debug_inject_stall(enable: bool) -> None:
     check(lib.gg_debug_inject_stall(1 if enable else 0))
+
+
+def device_status(stream=None) -> int:
+    """The library's status word of the current device (where launches given
+    no status word report a wait that gave up), after ``stream``'s queued work."""
+    out = ctypes.c_int()
+    check(lib.gg_device_status(_stream(stream), ctypes.byref(out)))
+    return out.value
+
+
+def clear_device_status(stream=None) -> None:
+    """Reset the library's status word of the current device to 0 (on ``stream``)."""
+    check(lib.gg_clear_device_status(_stream(stream)))
 
 
 # --------------------------------------------------------------------------- #

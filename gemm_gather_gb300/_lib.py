@@ -39,6 +39,7 @@ EXPORTS = (
     "gg_matmul_all_gather", "gg_matmul_all_gather_path", "gg_matmul_all_gather_check",
     "gg_set_claim_policy", "gg_get_claim_policy",
     "gg_set_wait_limit_ns", "gg_get_wait_limit_ns", "gg_debug_inject_stall",
+    "gg_device_status", "gg_clear_device_status",
     "gg_last_error", "gg_status_string", "gg_version",
 )
 
@@ -90,6 +91,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "gg_set_wait_limit_ns": ([u64], i32),
         "gg_get_wait_limit_ns": ([], u64),
         "gg_debug_inject_stall": ([i32], i32),
+        "gg_device_status": ([vp, ctypes.POINTER(i32)], i32),
+        "gg_clear_device_status": ([vp], i32),
         "gg_last_error": ([], ctypes.c_char_p),
         "gg_status_string": ([i32], ctypes.c_char_p),
         "gg_version": ([], i32),

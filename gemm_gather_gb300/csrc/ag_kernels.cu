@@ -606,7 +606,10 @@ bool ring_geometry(int64_t stage_raw, int programs, int target, int *npipe, int 
 // Claimed runs (GatherArgs::work) on the tensor-map path for the all-gather
 // and the all-to-all: about 64 runs per pipeline, 2 to 8 items a run; the
 // counter is zeroed on the launch's stream first (one memset of a few
-// microseconds).  Automatic choice: only launches that move at least
+// microseconds).  The counter is a heap workspace slot, or, for
+// gg_all_gather_noalloc, the library's static scratch array (gg_api.cu),
+// which every call on a device shares: that call relies on this memset to
+// start each launch from zero.  Automatic choice: only launches that move at least
 // kClaimAutoBytes over at least 3/4 of the SMs claim.  Below that every SM
 // gets the bandwidth it asks for, and claims only add their per-run cost
 // (measured on GB300: 5-7% slower at 16-64 programs, 8-16% faster at 128-148

@@ -139,6 +139,62 @@ bool checked_mul(int64_t a, int64_t b, int64_t *out)
     return true;
 }
 
+// Device address of a file-scope __device__ object on the current device.
+// Host code only holds a host-side stand-in for such an object, so its
+// device address is looked up (cudaGetSymbolAddress) once per device, with
+// that device current, and kept in cache[device].
+constexpr int kMaxDevices = 64;
+
+gg_status device_symbol(const void *symbol, void **cache, std::mutex &mu, const char *what,
+                        void **out)
+{
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices)
+        return fail(GG_ERR_UNSUPPORTED, "device %d: the library serves devices 0..%d", dev,
+                    kMaxDevices - 1);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!cache[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, symbol);
+        if (e != cudaSuccess)
+            return cuda_fail(e, what);
+        cache[dev] = p;
+    }
+    *out = cache[dev];
+    return GG_OK;
+}
+
+}  // namespace
+
+// The library's own status word (one int per device): launches whose caller
+// passes no dev_status report a bounded wait that gave up here, so a launch
+// that stopped early never goes unreported.  Read and cleared with
+// gg_device_status / gg_clear_device_status.
+static __device__ int g_library_status;
+
+namespace {
+
+std::mutex g_status_mu;
+void *g_status_ptr[kMaxDevices];
+
+gg_status library_status(int **out)
+{
+    void *p = nullptr;
+    gg_status st = device_symbol(&g_library_status, g_status_ptr, g_status_mu,
+                                 "cudaGetSymbolAddress of the library status word", &p);
+    *out = static_cast<int *>(p);
+    return st;
+}
+
+// The status word a launch reports to: the caller's, else the library's.
+gg_status resolve_status(int **status)
+{
+    return *status ? GG_OK : library_status(status);
+}
+
 }  // namespace
 
 extern "C" {
@@ -448,6 +504,9 @@ gg_status run_collective(const gg_heap *heap, int mode, int rank, const void *in
                                   &vec, &in_map, &maps, &launch);
     if (st != GG_OK || !launch)
         return st;
+    st = resolve_status(&a.status);
+    if (st != GG_OK)
+        return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // a workspace slot for launches that may claim runs (see prepare_claims)
     if (kind == kTma && mode != gg::kModePartitioned && a.claim_policy != GG_CLAIM_NEVER)
@@ -676,6 +735,9 @@ gg_status gg_matmul_all_gather_path(const gg_heap *heap, int rank, const void *A
                                  comm_programs, group, dev_status, &f, &maps, &launch);
     if (st != GG_OK || !launch)
         return st;
+    st = resolve_status(&f.status);
+    if (st != GG_OK)
+        return st;
     const char *why = nullptr;
     cudaError_t e = gg::launch_matmul_all_gather(f, maps, comm_programs, (int)path,
                                                  reinterpret_cast<cudaStream_t>(stream), &why);
@@ -730,6 +792,35 @@ gg_status gg_debug_inject_stall(int enable)
     return ok();
 }
 
+gg_status gg_device_status(gg_stream_t stream, int *host_out)
+{
+    if (!host_out)
+        return fail(GG_ERR_INVALID_ARG, "host_out is NULL");
+    int *word = nullptr;
+    gg_status st = library_status(&word);
+    if (st != GG_OK)
+        return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(host_out, word, sizeof(int), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "reading the library status word");
+    return ok();
+}
+
+gg_status gg_clear_device_status(gg_stream_t stream)
+{
+    int *word = nullptr;
+    gg_status st = library_status(&word);
+    if (st != GG_OK)
+        return st;
+    cudaError_t e = cudaMemsetAsync(word, 0, sizeof(int), reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "clearing the library status word");
+    return ok();
+}
+
 const char *gg_last_error(void) { return g_last_error.c_str(); }
 
 const char *gg_status_string(gg_status s)
@@ -758,8 +849,10 @@ int gg_version(void) { return 100; }
 // load-balanced tensor-map path lives in this file-scope device array instead
 // of a heap workspace.  It is a single region shared by every call on a
 // device, and holds the last call's counter until the next claiming call
-// zeroes it (one memset on that call's stream).  Every GPU that loads the
-// library keeps these bytes until the process exits.
+// zeroes it: prepare_claims (ag_kernels.cu) enqueues that memset on the
+// call's stream before the kernel, for a workspace slot and for this array
+// alike.  Every GPU that loads the library keeps these bytes until the
+// process exits.
 // ---------------------------------------------------------------------------
 constexpr size_t kNoAllocScratchBytes = 256;
 static __device__ __align__(256) unsigned long long g_noalloc_scratch[kNoAllocScratchBytes / 8];
@@ -768,31 +861,18 @@ static_assert(sizeof(unsigned long long) <= kNoAllocScratchBytes,
 
 namespace {
 
-constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
-unsigned long long *g_noalloc_dev_ptr[kNoAllocMaxDevices];
+void *g_noalloc_dev_ptr[kMaxDevices];
 
-// Device address of the scratch array on the current device: looked up once
-// per device (with that device current), then cached.
+// Device address of the scratch array on the current device: looked up at the
+// first call on each device (with that device current), then reused.
 gg_status noalloc_scratch(unsigned long long **out)
 {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= kNoAllocMaxDevices)
-        return fail(GG_ERR_UNSUPPORTED, "device %d: the allocation-free call serves devices 0..%d",
-                    dev, kNoAllocMaxDevices - 1);
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_dev_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess)
-            return cuda_fail(e, "cudaGetSymbolAddress of the static scratch array");
-        g_noalloc_dev_ptr[dev] = static_cast<unsigned long long *>(p);
-    }
-    *out = g_noalloc_dev_ptr[dev];
-    return GG_OK;
+    void *p = nullptr;
+    gg_status st = device_symbol(g_noalloc_scratch, g_noalloc_dev_ptr, g_noalloc_mu,
+                                 "cudaGetSymbolAddress of the static scratch array", &p);
+    *out = static_cast<unsigned long long *>(p);
+    return st;
 }
 
 }  // namespace
@@ -818,9 +898,12 @@ gg_status gg_all_gather_noalloc(const gg_heap *heap, int rank, const void *input
                         &in_map, &maps, &launch);
     if (st != GG_OK || !launch)
         return st;
+    st = resolve_status(&a.status);
+    if (st != GG_OK)
+        return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // the static counter stands in for a heap workspace slot; the launch
-    // zeroes it on `s` when it claims runs
+    // the static counter stands in for a heap workspace slot; when the launch
+    // claims runs, prepare_claims zeroes it on `s` before the kernel
     if (kind == kTma && a.claim_policy != GG_CLAIM_NEVER)
         a.work = scratch;
     cudaError_t e;

@@ -4,10 +4,12 @@
  *
  * C ABI.  Plain pointers and sizes only.  All device memory is owned by the
  * caller; the library never allocates device memory, and its only device
- * state is the 256-byte static counter of gg_all_gather_noalloc.  Every call
- * that launches work is asynchronous on the caller's
- * stream.  Errors found on the host are returned before anything is
- * launched; gg_last_error() then describes them.  No call aborts the process.
+ * state is two small static objects per device: the 256-byte counter array
+ * of gg_all_gather_noalloc and the int status word of launches given no
+ * status word (gg_device_status).  Every call that launches work is
+ * asynchronous on the caller's stream.  Errors found on the host are
+ * returned before anything is launched; gg_last_error() then describes
+ * them.  No call aborts the process.
  *
  * Logical ranks.  On one GPU the W ranks of a group are logical: H equal
  * partitions ("heaps") of one device allocation, reached through a table of
@@ -165,9 +167,12 @@ int gg_get_claim_policy(void);
  *   block_m in [1, 256], block_n >= 1, block_m*block_n*elem_size <= 32768.
  * comm_programs: number of persistent programs (CTAs) of the launch, 1..65535;
  *   for rank == -1 they share all world_size x tiles work items.
- * dev_status: nullable device int; if a bounded wait inside the kernel gives
- *   up, GG_ERR_TIMEOUT is stored there (first error wins; the caller zeroes
- *   it).  M == 0 or N == 0 launches nothing and returns GG_OK.
+ * dev_status: device int, or NULL; if a bounded wait inside the kernel gives
+ *   up (the kernel then stops early and part of the output may be left
+ *   unwritten), GG_ERR_TIMEOUT is stored there (first error wins; the caller
+ *   zeroes it).  With NULL it is stored in the library's status word of the
+ *   device instead (gg_device_status), so no early stop goes unreported.
+ *   M == 0 or N == 0 launches nothing and returns GG_OK.
  * Any alignment is accepted: 16-byte aligned pointers and pitches take the
  *   tensor-map or bulk-copy path, others a narrower vector path.  Results
  *   are identical.
@@ -201,6 +206,9 @@ gg_status gg_all_gather(const gg_heap *heap, int rank, const void *input, int64_
  * or repeat tiles -- order them on one stream.  The first call on each device
  * (with that device current) looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * The address found then is kept for the life of the process: after a
+ * cudaDeviceReset of that device it is stale, so do not call this entry
+ * point on a device that was reset after its first call.
  * ------------------------------------------------------------------------- */
 gg_status gg_all_gather_noalloc(const gg_heap *heap, int rank, const void *input, int64_t ld_in,
                                 void *output, int64_t ld_out, int64_t M, int64_t N,
@@ -323,6 +331,7 @@ gg_status gg_collective_check(gg_collective kind, const gg_heap *heap, int rank,
  *   By default they run as CTA pairs (comm_programs/2 clusters of two CTAs,
  *   a 256 x 256 output tile per pair); a single program runs alone on
  *   128 x 256 tiles.
+ * dev_status: as for gg_all_gather (NULL: the library's status word).
  * M, N or K == 0: nothing is launched, GG_OK (with K == 0 nothing is
  *   written either).
  * ------------------------------------------------------------------------- */
@@ -360,6 +369,20 @@ gg_status gg_matmul_all_gather_check(const gg_heap *heap, int rank, const void *
  * ------------------------------------------------------------------------- */
 gg_status gg_set_wait_limit_ns(uint64_t ns);
 uint64_t gg_get_wait_limit_ns(void);
+
+/* The library's status word of the current device: where launches whose
+ * caller passed dev_status == NULL store GG_ERR_TIMEOUT when a bounded wait
+ * gives up (first error wins; 0 while no such launch stopped early).
+ * gg_device_status waits for `stream` to finish the work queued on it so far,
+ * then copies the word to *host_out (host memory); gg_clear_device_status
+ * enqueues its reset to 0 on `stream`.  Both look the word's address up once
+ * per device (cudaGetSymbolAddress, with that device current) at their first
+ * use, or at the first launch given no status word; make that first use
+ * before any stream capture, and do not use the word on a device after a
+ * cudaDeviceReset of it.  Every launch on a device without a status word of
+ * its own shares this one word. */
+gg_status gg_device_status(gg_stream_t stream, int *host_out);
+gg_status gg_clear_device_status(gg_stream_t stream);
 
 /* Test hook for the bounded waits (failure detection without a GPU fault).
  * While enabled, launches of the bulk all-gather path and of the fused

@@ -92,3 +92,56 @@ def test_fused_wait_limit_reports_timeout(oracle, short_waits, path):
                              B.view(torch.int16).numpy().view(np.uint16), lay.out_off, N, M, N, K,
                              0, (0, 1, W))
     assert np.array_equal(got, host), first_diff(got, host, lay)
+
+
+@pytest.mark.parametrize("kind", ["bulk", "tma", "1sm", "2sm"])
+def test_timeout_without_status_word_is_reported(oracle, short_waits, kind):
+    """A launch given no status word (NULL) reports a wait that gave up in the
+    library's status word of the device: no early stop goes unreported.  After
+    clearing it, the same launch runs normally, leaves the word at 0 and gives
+    the oracle's heap."""
+    import gemm_gather_gb300 as gg
+    fused = kind in ("1sm", "2sm")
+    if fused:
+        W, M, N, K = 2, 512, 1024, 2048
+        lay = hi.make_layout(W, W, M, N, 2, ld_in=K)
+        host = hi.sentinel_heap(lay)
+        gen = gg_inputs.generator(2)
+        for h in range(W):
+            a = gg_inputs.integers((M, K), -2, 2, torch.float16, gen)
+            hi.put_block(host, lay, h, a.view(torch.int16).numpy(), lay.in_off, K)
+        B = gg_inputs.integers((K, N), -2, 2, torch.float16, gen)
+        Bd = B.to("cuda")
+    else:
+        lay, host = _gather_heap()
+    sh = device_heap(lay, host)
+
+    def launch():
+        if fused:
+            gg.matmul_all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), K, Bd, N,
+                                 sh.ptr(0, lay.out_off), N, M, N, K, torch.float16,
+                                 gg.FUSED_TILE, 8, (0, 1, W), status=None, path=kind)
+        else:
+            gg.all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), lay.ld_in, sh.ptr(0, lay.out_off),
+                          lay.ld_out, lay.M, lay.N, torch.float16, (8, 256), 4, (0, 1, 4),
+                          status=None, path=kind)
+
+    gg.clear_device_status()
+    assert gg.device_status() == 0
+    launch()
+    assert gg.device_status() == TIMEOUT
+    gg.debug_inject_stall(False)
+    gg.set_wait_limit_ns(0)
+    gg.clear_device_status()
+    assert gg.device_status() == 0
+    launch()
+    got = download(sh)
+    assert gg.device_status() == 0
+    if fused:
+        oracle.matmul_all_gather(host, lay.part_bytes, lay.in_off, K,
+                                 B.view(torch.int16).numpy().view(np.uint16), lay.out_off, N, M,
+                                 N, K, 0, (0, 1, W))
+    else:
+        oracle.all_gather(host, lay.part_bytes, lay.in_off, lay.ld_in, lay.out_off, lay.ld_out,
+                          lay.M, lay.N, 2, (0, 1, 4))
+    assert np.array_equal(got, host), first_diff(got, host, lay)
