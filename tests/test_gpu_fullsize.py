@@ -7,10 +7,11 @@ each case checks
   row block i equals member i's input (a gather is a copy; fused: all W copies
   of each block are bit-identical), and every byte outside the outputs keeps
   its sentinel (guards, inactive heaps);
-* sampled rows against the oracle: the oracle gathers (or multiplies, in
-  float64) the sampled rows of every rank, and those rows of every member's
-  output must match (bit-exact for the gather, the float64 tolerance for the
-  fused product).
+* rows against the oracle: the oracle gathers (or multiplies, in float64)
+  sampled rows of every rank, and those rows of every member's output must
+  match (bit-exact for the gather, the float64 tolerance for the fused
+  product); the fused product at M_local=1024 is compared on every row, the
+  larger fused shapes on 256 seeded rows per rank.
 Inputs are drawn on the GPU from a seeded generator (same distributions as
 the benchmark); the sampled rows are copied to the host for the oracle.
 """
@@ -121,6 +122,12 @@ def test_gather_full_size(oracle, case):
         assert np.array_equal(got, want), d
 
 
+# Rows of every rank compared with the float64 oracle: all of them at
+# M_local=1024 (481 GFLOP of oracle work), a seeded sample of 256 (plus the
+# first and last row) at the larger shapes.
+FUSED_ALL_ROWS_UP_TO = 1024
+FUSED_SAMPLE_ROWS = 256
+
 FUSED_CASES = [
     # (W, group, M, dtype, path)
     (8, (0, 1, 8), 1024, torch.float16, "auto"),
@@ -130,6 +137,7 @@ FUSED_CASES = [
     (8, (0, 1, 8), 16384, torch.float16, "auto"),
     (8, (0, 1, 8), 16384, torch.bfloat16, "auto"),
     (4, (0, 2, 4), 4096, torch.float16, "auto"),
+    (4, (0, 2, 4), 16384, torch.float16, "auto"),
     (4, (0, 2, 4), 16384, torch.bfloat16, "auto"),
 ]
 
@@ -172,8 +180,11 @@ def test_fused_full_size(oracle, case):
             _assert_sentinel(p[out_off + out_bytes:], f"heap {h} back guard")
         else:
             _assert_sentinel(p, f"inactive heap {h}")
-    # sampled rows of every rank against the float64 oracle
-    rows = _rows_sample(M, 3, seed=M)
+    # rows of every rank (all of them, or a seeded sample) against the float64 oracle
+    if M <= FUSED_ALL_ROWS_UP_TO:
+        rows = np.arange(M, dtype=np.int64)
+    else:
+        rows = _rows_sample(M, FUSED_SAMPLE_ROWS, seed=M + 17 * W + int(dtype == torch.bfloat16))
     Bbits = B.view(torch.int16).cpu().numpy().view(np.uint16)
     fmt = 0 if dtype == torch.float16 else 1
     out = ref_out.view(dtype)
