@@ -1,14 +1,19 @@
 #!/usr/bin/env python
 """Benchmark of the hot path on one GB300 (or N replicas under torchrun).
 
-One step = one pass of the whole path over one batch of synthetic inputs:
-  1. persistent all-gather: W=8 logical ranks, 4096 x 4096 f16 per rank
-     (uniform[-1,1]), explicit tile 8x256, 148 programs, local copy first
-     then peers rotated (tensor-map path, runs of tiles claimed per program);
-  2. fused matmul + all-gather: W=8, M_local=1024, N=3584, K=8192, f16 in,
-     f32 accumulate, f16 out, 128x256 tcgen05 tiles, inputs normal(0,1)/sqrt(K).
-Every rank's 8 logical ranks live in one symmetric heap on its own GPU; the
-per-step working set (about 3 GB) is far larger than L2.
+One step = one pass of the whole path over one batch of synthetic inputs, at
+the largest configurations of the workload (the default, ``--preset largest``):
+  1. persistent all-gather: W=8 logical ranks, 16384 x 8192 f32 per rank
+     (normal(0,1)), explicit tile 8x256, 148 programs, local copy first then
+     peers rotated (tensor-map path, runs of tiles claimed per program);
+  2. fused matmul + all-gather: W=8, M_local=16384, N=3584, K=8192, f16 in,
+     f32 accumulate, f16 out, 128x256 tcgen05 tiles (256x256 per CTA pair),
+     inputs normal(0,1)/sqrt(K).
+``--preset small`` runs the smaller step instead: the W=8 4096 x 4096 f16
+all-gather (uniform[-1,1]) and the fused product at M_local=1024.  Every
+rank's 8 logical ranks live in one symmetric heap on its own GPU; the
+per-step working set (about 48 GB; 3 GB for the small step) is far larger
+than L2.
 
 The metric is the step's roofline time (gather bytes at the measured HBM
 peak + fused FLOPs at the measured dense f16 tensor peak) as a percentage of
@@ -91,11 +96,18 @@ class FusedCfg:
 
 ES = {"f16": 2, "bf16": 2, "f32": 4}
 L2_BYTES = 126 << 20  # GB300 L2
-# The benchmark's all-gather takes the library's automatic choice: the
+# The benchmark's all-gathers take the library's automatic choice: the
 # tensor-map path, which at 148 programs claims runs of tiles from the heap's
 # workspace (load balancing across SMs).
-GATHER = GatherCfg()
-FUSED = FusedCfg()
+GATHER = GatherCfg()                 # W=8 4096x4096 f16: the budget / variant sweeps' base
+FUSED = FusedCfg()                   # W=8 M_local=1024
+GATHER_LARGEST = GatherCfg(M=16384, N=8192, dtype="f32", values="normal")
+FUSED_LARGEST = FusedCfg(M=16384)
+PRESETS = {"largest": (GATHER_LARGEST, FUSED_LARGEST), "small": (GATHER, FUSED)}
+
+# The end-to-end variant that reads every member's copy of the outputs back
+# runs only while those copies fit this much pinned host memory.
+E2E_ALL_COPIES_MAX_BYTES = 8 << 30
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 F16_PER_BF16 = 1.0  # nominal dense f16 : bf16 tensor rate
@@ -158,17 +170,19 @@ def source_sha(name: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def traffic_for(kernel: str, src: str):
-    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or
-    None when the kernel source changed since the counters were taken."""
+def traffic_for(kernel: str, src: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` on `workload` from the committed ncu
+    summary, or None when no entry covers that workload or the kernel source
+    changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        t = json.load(f).get(kernel)
-    if not t or t.get("source_sha") != source_sha(src):
-        return None
-    return t.get("bytes_per_launch")
+        entries = json.load(f).get(kernel) or []
+    for t in entries if isinstance(entries, list) else [entries]:
+        if t.get("bench_workload") == workload and t.get("source_sha") == source_sha(src):
+            return t.get("bytes_per_launch")
+    return None
 
 
 class ClockSampler:
@@ -534,6 +548,58 @@ def launch_gather(gg, g: GatherCfg, sh, offs, status, dt, stream):
         gg.all_gather(*args, status=status, stream=stream, path=g.path)
 
 
+FUSED_REL_TOL = 5e-3  # max |gpu - ref| <= 5e-3 * RMS(ref row) (+ half an ulp of the output type)
+
+
+def check_point(g: GatherCfg | None, f: FusedCfg | None, sh, offs, Bd) -> str:
+    """Check the outputs a sweep point left in the heap; raise on a mismatch.
+
+    Gather family: every member's row block i is, bit for bit, member i's input
+    (all-to-all: member i's block d, for member d).  Fused: the W copies of the
+    output are bit-identical, and three rows of every rank (first, middle,
+    last) are within 5e-3 * RMS(row) plus half an output ulp of a float64
+    product computed on the host with torch."""
+    import torch
+
+    import gg_inputs
+    if g is not None:
+        dt = gg_inputs.DTYPES[g.dtype]
+        bits = {2: torch.int16, 4: torch.int32}[g.es]
+        W, M, N = g.W, g.M, g.N
+        in_rows = W * M if g.kind == "all_to_all" else M
+        ins = {h: sh.view(h, offs["g_in"], in_rows, N, N, dt).view(bits) for h in g.members()}
+        for d_idx, d in enumerate(g.members()):
+            out = sh.view(d, offs["g_out"], W * M, N, N, dt).view(bits)
+            for i, h in enumerate(g.members()):
+                want = ins[h][d_idx * M:(d_idx + 1) * M] if g.kind == "all_to_all" else ins[h]
+                if not torch.equal(out[i * M:(i + 1) * M], want):
+                    raise RuntimeError(f"{g.describe()}: member {d} block {i} differs")
+        return "every block bit-exact"
+    dt = gg_inputs.DTYPES[f.dtype]
+    W, M, N, K = f.W, f.M, f.N, f.K
+    first = sh.view(f.members()[0], offs["f_out"], W * M, N, N, dt)
+    for d in f.members()[1:]:
+        if not torch.equal(sh.view(d, offs["f_out"], W * M, N, N, dt).view(torch.int16),
+                           first.view(torch.int16)):
+            raise RuntimeError(f"{f.describe()}: member {d}'s copy differs from member "
+                               f"{f.members()[0]}'s")
+    rows = sorted({0, M // 2, M - 1})
+    b64 = Bd.to("cpu", torch.float64)
+    mant = 10 if f.dtype == "f16" else 7
+    for i, h in enumerate(f.members()):
+        a = sh.view(h, offs["f_a"], M, K, K, dt)[rows].to("cpu", torch.float64)
+        ref = a @ b64
+        got = first[[i * M + r for r in rows]].to("cpu", torch.float64)
+        rms = ref.pow(2).mean(dim=1, keepdim=True).sqrt()
+        mag = torch.maximum(ref.abs(), got.abs()).clamp_min(2.0 ** -14)
+        half_ulp = torch.exp2(torch.floor(torch.log2(mag)) - mant - 1)
+        bad = (got - ref).abs() > FUSED_REL_TOL * rms + half_ulp
+        if bool(bad.any()):
+            raise RuntimeError(f"{f.describe()}: rank {h}: {int(bad.sum())} values outside "
+                               "the tolerance")
+    return "copies bit-identical; 3 rows per rank within tolerance of a float64 product"
+
+
 def run_sweep(args):
     """Time each point of a sweep in this process; one JSON line per point."""
     import torch
@@ -589,8 +655,10 @@ def run_sweep(args):
         ms = statistics.median(runs)
         if int(status.item()) != 0:
             raise RuntimeError(f"device status {int(status.item())}")
+        checked = check_point(g, f, sh, offs, Bd)
         rec = {"sweep": args.sweep, "workload": (g or f).describe(), "ms": ms, "steps": steps,
-               "runs_ms": runs, "roofline_ms": 1e3 * work, "frac": 1e3 * work / ms}
+               "runs_ms": runs, "roofline_ms": 1e3 * work, "frac": 1e3 * work / ms,
+               "checked": checked}
         moved = gather_bytes(g) if g else fused_bytes(f)
         if moved < 2 * L2_BYTES and args.sweep != "small":
             # small enough to be partly L2-resident between back-to-back launches:
@@ -649,6 +717,9 @@ def main():
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--workload", default="step", choices=["step", "gather", "fused"],
                     help="step: the all-gather then the fused kernel; or one of them alone")
+    ap.add_argument("--preset", default="largest", choices=sorted(PRESETS),
+                    help="largest: W=8 16384x8192 f32 all-gather + fused M_local=16384 "
+                    "(default); small: W=8 4096x4096 f16 all-gather + fused M_local=1024")
     ap.add_argument("--gather", default="", help="overrides, e.g. W=4,M=1024,N=8192,dtype=f32,"
                     "tile=16x128,programs=128,group=1:2,values=normal,path=bulk")
     ap.add_argument("--fused", default="", help="overrides, e.g. M=16384,dtype=bf16,group=0:2,W=4")
@@ -673,8 +744,9 @@ def main():
     args.warmup = max(args.warmup, 3)
     if args.sweep:
         return run_sweep(args)
-    g = parse_cfg(args.gather, GATHER) if args.workload in ("step", "gather") else None
-    f = parse_cfg(args.fused, FUSED) if args.workload in ("step", "fused") else None
+    base_g, base_f = PRESETS[args.preset]
+    g = parse_cfg(args.gather, base_g) if args.workload in ("step", "gather") else None
+    f = parse_cfg(args.fused, base_f) if args.workload in ("step", "fused") else None
     peaks, peak_src = load_peaks()
     if args.impl == "reference":
         return run_reference(args, peaks, peak_src, g, f)
@@ -764,17 +836,27 @@ def main():
     # ---- end to end through the C ABI, host buffers, copies in the timed region
     e2e = None
     if args.e2e_steps > 0:
-        if host is None:  # inputs were drawn on the device: stage them to the host once
-            host = {"g_in": {}, "f_a": {}}
+        if host is None:
+            # inputs were drawn on the device: stage them once into pinned host memory
+            def pinned_copy(t):
+                p = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                p.copy_(t)
+                return p
+
+            pin = {"g_in": {}, "f_a": {}}
             if g:
                 for h in g.members():
-                    host["g_in"][h] = sh.view(h, offs["g_in"], g_in_rows, g.N, g.N, gdt).cpu()
+                    pin["g_in"][h] = pinned_copy(sh.view(h, offs["g_in"], g_in_rows, g.N, g.N,
+                                                         gdt))
             if f:
                 for h in f.members():
-                    host["f_a"][h] = sh.view(h, offs["f_a"], f.M, f.K, f.K, fdt).cpu()
-                host["B"] = Bd.cpu()
-        pin = {k: {h: x.pin_memory() for h, x in v.items()} for k, v in host.items() if k != "B"}
-        pin_b = host["B"].pin_memory() if f else None
+                    pin["f_a"][h] = pinned_copy(sh.view(h, offs["f_a"], f.M, f.K, f.K, fdt))
+            pin_b = pinned_copy(Bd) if f else None
+        else:
+            pin = {k: {h: x.pin_memory() for h, x in v.items()} for k, v in host.items()
+                   if k != "B"}
+            pin_b = host["B"].pin_memory() if f else None
+        host = None
 
         # The step's result: the gathered outputs.  Every member holds an identical
         # copy (what the parity tests check), so the result is read from the first
@@ -789,7 +871,6 @@ def main():
         first_g = g.members()[:1] if g else []
         first_f = f.members()[:1] if f else []
         outs = [out_set(first_g, first_f), out_set(first_g, first_f)]
-        outs_all = [out_set(g.members() if g else [], f.members() if f else [])] * 2
         h2d = sum(x.numel() * x.element_size() for v in pin.values() for x in v.values()) + \
             (pin_b.numel() * 2 if f else 0)
 
@@ -797,7 +878,11 @@ def main():
             return sum(x.numel() * x.element_size() for d in oset for x in d.values())
 
         d2h = nbytes(outs[0])
-        d2h_all = nbytes(outs_all[0])
+        # every member's copy as well, while it fits a bounded pinned buffer
+        d2h_all = (g.W * g.W * g.M * g.N * g.es if g else 0) + \
+            (f.W * f.W * f.M * f.N * 2 if f else 0)
+        outs_all = ([out_set(g.members() if g else [], f.members() if f else [])] * 2
+                    if d2h_all <= E2E_ALL_COPIES_MAX_BYTES else None)
 
         def copy_in(heap, b_dev):
             if g:
@@ -879,10 +964,15 @@ def main():
             return max_over_ranks(p0.elapsed_time(p1) / e2e_steps, dev)
 
         e2e_ms = timed_pipeline(outs)
-        all_ms = timed_pipeline(outs_all)
+        if outs_all is not None:
+            all_copies = {"d2h_bytes_per_step": d2h_all, "ms_per_step": timed_pipeline(outs_all)}
+        else:
+            all_copies = {"d2h_bytes_per_step": d2h_all, "ms_per_step": None,
+                          "skipped": f"more than {E2E_ALL_COPIES_MAX_BYTES >> 30} GiB of pinned "
+                                     "host memory"}
         e2e = {"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": e2e_steps, "serial_ms_per_step": serial_ms,
-               "all_copies": {"d2h_bytes_per_step": d2h_all, "ms_per_step": all_ms},
+               "all_copies": all_copies,
                "path": ("pinned host -> heap (cudaMemcpyAsync) -> C-ABI calls -> pinned host; "
                         "every member's inputs copied in, the gathered outputs read back from "
                         "member 0 (all members hold identical copies); steps pipelined over two "
@@ -916,13 +1006,13 @@ def main():
         k = kernels["all_gather"]
         roof = {"kernel": k["kernel"], "bound": "hbm", "achieved": k["GB/s"], "peak": hbm_peak,
                 "unit": "GB/s", "frac": k["frac"],
-                "traffic": traffic_for(k["kernel"], "ag_kernels.cu"),
+                "traffic": traffic_for(k["kernel"], "ag_kernels.cu", g.describe()),
                 "per_unit": "bytes = W*M*N*s reads + W^2*M*N*s writes per launch"}
     else:
         k = kernels["matmul_all_gather"]
         roof = {"kernel": k["kernel"], "bound": "tensor", "achieved": k["TFLOP/s"],
                 "peak": tc_peak, "unit": "TFLOP/s", "frac": k["frac"],
-                "traffic": traffic_for(k["kernel"], "mag_kernel.cu"),
+                "traffic": traffic_for(k["kernel"], "mag_kernel.cu", f.describe()),
                 "per_unit": "FLOPs = 2*W*M*N*K per launch"}
     roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peak_src == "measured"
                            else "fallback")
