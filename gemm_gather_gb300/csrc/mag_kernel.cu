@@ -20,7 +20,10 @@
 //     round to f16/bf16 and write each value once into shared memory as
 //     32-row x 64-column boxes in the 128-byte swizzled layout, then one TMA
 //     tensor store (cp.async.bulk.tensor shared->global) per box and
-//     destination: the local copy first, then the peers in rotated order.
+//     destination: the local copy first, then the peers in rotated order,
+//     one destination per time slot spread over most of a tile period (store
+//     pacing: the CTAs' epilogues would otherwise coincide and flood DRAM
+//     with writes while the next tile's operands load).
 //     The accumulator is released right after it has been read, so the next
 //     tile's MMAs overlap this tile's stores.
 // Each destination's tensor map is built on the host from the heap-bases
@@ -60,6 +63,11 @@ constexpr int kTmemCols = 512;
 constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
 constexpr int kBox = 32 * 64 * 2;               // 4 KB: one epilogue store box, 32 rows x 64 cols
+// Store pacing: the W copies of a tile go out in slots spread over this share
+// of the previous tile's period (see the epilogue), and a period is capped at
+// kPaceMaxPeriodNs so that a stalled tile cannot stretch the next one's waits.
+constexpr uint64_t kPacePct = 70;
+constexpr uint64_t kPaceMaxPeriodNs = 2000000ull;
 
 // Geometry of the 1-SM (CG = 1) and 2-SM (CG = 2) variants.  With CG = 2 a
 // CTA pair computes a 256 x 256 tile: each CTA holds its 128 rows of A and
@@ -627,8 +635,18 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         const uint64_t pol_c = ptx::policy_evict_first();  // output: written once, never read
         constexpr int kOps = G::kEpiBoxes;                   // stores per destination per pass
+        constexpr int kPasses = BN / G::kEpiCols;
         int64_t lt = 0;
         bool ok = true;
+        // Store pacing.  Every CTA runs its K loop in step with the others, so
+        // their epilogues would all fire at once and put a whole wave of W-fold
+        // output writes on DRAM in a burst that starves the operand loads.
+        // Instead a tile's W x kPasses store groups leave in evenly spaced
+        // slots across kPacePct of the previous tile's period (the first
+        // tile's period counts from the kernel's start), overlapping the next
+        // tile's mainloop; a CTA's last tile, with no mainloop behind it, is
+        // not paced.
+        uint64_t prev_ready = ptx::globaltimer();
         for (int64_t t = unit; t < total; t += nunits, ++lt) {
             const TileCoord c = tile_coord(a, t, tiles_m, tiles_n);
             const int acc = (int)(lt & 1);
@@ -639,6 +657,13 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
                 ok = false;
                 break;
             }
+            const uint64_t t_ready = ptx::globaltimer();
+            uint64_t period = t_ready - prev_ready;
+            period = period > kPaceMaxPeriodNs ? kPaceMaxPeriodNs : period;
+            prev_ready = t_ready;
+            // time between two store groups of this tile (0: no pacing)
+            const uint64_t slot =
+                t + nunits < total ? period * kPacePct / 100u / (uint64_t)(kPasses * a.W) : 0;
             tc_fence_after();
             const uint32_t t_addr = tmem + lane_addr + (uint32_t)(acc * BN);
             // first row of this warp's boxes, within the source's row block
@@ -689,7 +714,23 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
                 const int col0 = c.tn * BN + pass;
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
-                if (row0 < a.M) {
+                if (row0 < a.M && slot != 0) {
+                    // one destination per slot: lane b stores box b
+                    const uint64_t first = (uint64_t)(pass / G::kEpiCols) * (uint64_t)a.W;
+                    for (int j = 0; j < a.W; ++j) {
+                        const uint64_t due = t_ready + slot * (first + (uint64_t)j);
+                        while (ptx::globaltimer() < due && !*abort_flag)
+                            __nanosleep(256);
+                        const int col = col0 + lane * 64;
+                        if (lane < kOps && col < a.N) {
+                            int i = c.g + j;
+                            if (i >= a.W)
+                                i -= a.W;
+                            tma_store_3d(&out.map[i], warp_stage + (uint32_t)(lane * kBox), col,
+                                         row0, c.g, pol_c);
+                        }
+                    }
+                } else if (row0 < a.M) {
                     for (int op = lane; op < a.W * kOps; op += 32) {
                         const int j = op / kOps;
                         const int b = op - j * kOps;
