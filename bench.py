@@ -994,13 +994,16 @@ def main():
         kname = {"vector": "ag_vec_kernel", "bulk": "ag_bulk_kernel"}.get(g.path, "ag_tma_kernel")
         kernels["all_gather"] = {"kernel": kname, "ms": g_ms, "GB/s": g_gbs,
                                  "roofline_ms": 1e3 * t_rg, "frac": g_gbs / hbm_peak,
-                                 "bound": "hbm", "algorithmic_bytes": gather_bytes(g)}
+                                 "bound": "hbm", "algorithmic_bytes": gather_bytes(g),
+                                 "traffic": traffic_for(kname, "ag_kernels.cu", g.describe())}
     if f:
         f_tfs = fused_flops(f) / (f_ms * 1e-3) / 1e12
         fk = "mag1_kernel" if (f.path == "1sm" or f.programs < 2) else "mag2_kernel"
         kernels["matmul_all_gather"] = {"kernel": fk, "ms": f_ms, "TFLOP/s": f_tfs,
                                         "roofline_ms": 1e3 * t_rf, "frac": f_tfs / tc_peak,
                                         "bound": "tensor", "algorithmic_flops": fused_flops(f),
+                                        "algorithmic_bytes": fused_bytes(f),
+                                        "traffic": traffic_for(fk, "mag_kernel.cu", f.describe()),
                                         "programs": f.programs}
     if g and (not f or g_ms >= f_ms):
         k = kernels["all_gather"]
