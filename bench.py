@@ -513,6 +513,10 @@ def sweep_points(name: str):
             pts.append((replace(GATHER, programs=p, kind="all_to_all", path="auto"), None))
         for p in (8, 16, 32, 64, 148):  # W single-rank launches in turn
             pts.append((replace(GATHER, programs=p, kind="ranks"), None))
+    elif name == "cublas":  # the fused kernel and cuBLAS on the plain GEMM of the same size
+        for M in (1024, 4096, 16384):
+            for dt in ("f16", "bf16"):
+                pts.append((None, replace(FUSED, M=M, dtype=dt, path="2sm")))
     elif name == "fused":  # 8 ranks, M_local 1024/4096/16384, f16 and bf16, + subgroup (0,2,4)
         for path in ("2sm", "1sm"):
             for M in (1024, 4096, 16384):
@@ -634,24 +638,29 @@ def run_sweep(args):
 
         t_rg, t_rf = roofline_times(peaks, g, f)
         work = t_rg + t_rf
-        steps = int(max(5, min(args.steps, 0.5 / max(work, 1e-6))))
-        for _ in range(args.warmup):
-            launch()
-        torch.cuda.synchronize(dev)
-        clocks = ClockSampler(dev.index or 0, None) if args.sweep_clocks else None
-        if clocks:
-            clocks.start()
-            steps = max(steps, int(1.0 / max(work, 1e-6)))  # at least ~1 s under load
-        runs = []
-        for _ in range(max(1, args.repeats)):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(steps):
-                launch()
-            e1.record()
+
+        def timed(fn):
+            """(median ms per launch over the repeats, launches per run, clocks)"""
+            steps = int(max(5, min(args.steps, 0.5 / max(work, 1e-6))))
+            for _ in range(args.warmup):
+                fn()
             torch.cuda.synchronize(dev)
-            runs.append(e0.elapsed_time(e1) / steps)
-        clk = clocks.stop() if clocks else None
+            clocks = ClockSampler(dev.index or 0, None) if args.sweep_clocks else None
+            if clocks:
+                clocks.start()
+                steps = max(steps, int(1.0 / max(work, 1e-6)))  # at least ~1 s under load
+            runs = []
+            for _ in range(max(1, args.repeats)):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(steps):
+                    fn()
+                e1.record()
+                torch.cuda.synchronize(dev)
+                runs.append(e0.elapsed_time(e1) / steps)
+            return runs, steps, (clocks.stop() if clocks else None)
+
+        runs, steps, clk = timed(launch)
         ms = statistics.median(runs)
         if int(status.item()) != 0:
             raise RuntimeError(f"device status {int(status.item())}")
@@ -703,6 +712,19 @@ def run_sweep(args):
             rec["GB/s"] = gather_bytes(g) / (ms * 1e-3) / 1e9
         else:
             rec["TFLOP/s"] = fused_flops(f) / (ms * 1e-3) / 1e12
+        if args.sweep == "cublas":
+            # cuBLAS (torch.matmul) on the plain GEMM of the same total size, one
+            # output copy, timed the same way right after, on the same GPU
+            dt = gg_inputs.DTYPES[f.dtype]
+            a_all = torch.randn(f.W * f.M, f.K, device=dev, dtype=torch.float32).mul_(
+                f.K ** -0.5).to(dt)
+            c_all = torch.empty(f.W * f.M, f.N, device=dev, dtype=dt)
+            c_runs, _, c_clk = timed(lambda: torch.matmul(a_all, Bd, out=c_all))
+            c_ms = statistics.median(c_runs)
+            rec["cublas"] = {"gemm": f"{f.W * f.M}x{f.N}x{f.K} {f.dtype}", "ms": c_ms,
+                             "TFLOP/s": fused_flops(f) / (c_ms * 1e-3) / 1e12, "clocks": c_clk}
+            rec["vs_cublas"] = c_ms / ms
+            del a_all, c_all
         print(json.dumps(rec), flush=True)
         del sh, Bd, status
         torch.cuda.empty_cache()
@@ -729,7 +751,7 @@ def main():
                     help="draw inputs on the GPU (seeded) instead of the CPU")
     ap.add_argument("--clocks-out", default=None)
     ap.add_argument("--sweep", default=None,
-                    choices=["budget", "gather", "fused", "variants", "small"],
+                    choices=["budget", "gather", "fused", "variants", "small", "cublas"],
                     help="time every point of a configuration sweep (one JSON line each)")
     ap.add_argument("--only", default="", help="sweep: run only points whose description "
                     "contains one of these '|'-separated substrings")
@@ -932,6 +954,8 @@ def main():
         ev_cmp = [torch.cuda.Event() for _ in range(2)]
         ev_out = [torch.cuda.Event() for _ in range(2)]
 
+        run_kernels = [True]
+
         def pipelined(n, out_sets):
             for i in range(n):
                 b = i % 2
@@ -945,7 +969,8 @@ def main():
                     s_cmp.wait_event(ev_in[b])
                     if i >= 2:
                         s_cmp.wait_event(ev_out[b])  # step i-2's outputs are copied out
-                    launch_step(heap, b_dev, s_cmp)
+                    if run_kernels[0]:
+                        launch_step(heap, b_dev, s_cmp)
                     ev_cmp[b].record(s_cmp)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(ev_cmp[b])
@@ -964,6 +989,10 @@ def main():
             return max_over_ranks(p0.elapsed_time(p1) / e2e_steps, dev)
 
         e2e_ms = timed_pipeline(outs)
+        # the same pipelined copies with no kernels: the host link's share of the step
+        run_kernels[0] = False
+        copies_ms = timed_pipeline(outs)
+        run_kernels[0] = True
         if outs_all is not None:
             all_copies = {"d2h_bytes_per_step": d2h_all, "ms_per_step": timed_pipeline(outs_all)}
         else:
@@ -972,6 +1001,9 @@ def main():
                                      "host memory"}
         e2e = {"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": e2e_steps, "serial_ms_per_step": serial_ms,
+               "copies_only": {"ms_per_step": copies_ms,
+                               "GB/s": (h2d + d2h) / (copies_ms * 1e-3) / 1e9,
+                               "note": "the same pipelined host<->device copies with no kernels"},
                "all_copies": all_copies,
                "path": ("pinned host -> heap (cudaMemcpyAsync) -> C-ABI calls -> pinned host; "
                         "every member's inputs copied in, the gathered outputs read back from "
