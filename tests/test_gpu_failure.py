@@ -42,11 +42,13 @@ def test_gather_wait_limit_reports_timeout(oracle, short_waits, path):
     lay, host = _gather_heap()
     sh = device_heap(lay, host)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gg.clear_device_status()
     gg.all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), lay.ld_in, sh.ptr(0, lay.out_off),
                   lay.ld_out, lay.M, lay.N, torch.float16, (8, 256), 4, (0, 1, 4),
                   status=status, path=path)
     torch.cuda.synchronize()
     assert int(status.item()) == TIMEOUT
+    assert gg.device_status() == 0  # the caller's word got it; the library's stays clear
     # the context is intact: a normal launch gives the oracle's heap
     gg.debug_inject_stall(False)
     gg.set_wait_limit_ns(0)
@@ -75,11 +77,13 @@ def test_fused_wait_limit_reports_timeout(oracle, short_waits, path):
     sh = device_heap(lay, host)
     Bd = B.to("cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gg.clear_device_status()
     gg.matmul_all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), K, Bd, N, sh.ptr(0, lay.out_off), N,
                          M, N, K, torch.float16, gg.FUSED_TILE, 8, (0, 1, W), status=status,
                          path=path)
     torch.cuda.synchronize()
     assert int(status.item()) == TIMEOUT
+    assert gg.device_status() == 0  # the caller's word got it; the library's stays clear
     gg.debug_inject_stall(False)
     gg.set_wait_limit_ns(0)
     status.zero_()
