@@ -48,11 +48,20 @@ def _ptr(x) -> int | None:
     return int(x)
 
 
+# torch's own accessors of the current device and its current raw stream
+# (what torch.cuda.current_stream() wraps, without building a Stream object:
+# a few microseconds per call that small launches would otherwise pay)
+_current_device = getattr(torch._C, "_cuda_getDevice", None)
+_current_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream) -> int | None:
     if stream is None:
-        if torch.cuda.is_available() and torch.cuda.is_initialized():
-            return torch.cuda.current_stream().cuda_stream or None
-        return None
+        if not torch.cuda.is_initialized():
+            return None  # the legacy default stream
+        if _current_device is not None and _current_raw_stream is not None:
+            return _current_raw_stream(_current_device()) or None
+        return torch.cuda.current_stream().cuda_stream or None
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream or None
     return int(stream) or None

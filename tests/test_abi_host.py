@@ -263,3 +263,14 @@ def test_next_collectives_reject(heap, kind, kw, status):
     with pytest.raises(gg.GGError) as e:
         coll(heap, kind, **kw)
     assert e.value.status == status, str(e.value)
+
+
+def test_binding_stream_argument():
+    """The binding passes an explicit stream through as its handle, and the
+    legacy default stream (NULL) while torch has not initialised CUDA."""
+    import torch
+    from gemm_gather_gb300 import _stream
+    assert _stream(0x1234) == 0x1234
+    assert _stream(0) is None
+    if not torch.cuda.is_initialized():
+        assert _stream(None) is None

@@ -162,3 +162,15 @@ def test_repeated_launches_are_idempotent(oracle):
     """Launching the same gather twice leaves the same heap (no state carried)."""
     _run_case(oracle, 4, (0, 1, 4), 48, 512, 2, (8, 256), 8)
     _run_case(oracle, 4, (0, 1, 4), 48, 512, 2, (8, 256), 8, seed=3)
+
+
+def test_binding_uses_torch_current_stream():
+    """With no stream given, the binding launches on torch's current stream of
+    the current device (the raw handle torch.cuda.current_stream() wraps)."""
+    from gemm_gather_gb300 import _stream
+    torch.cuda.init()
+    s = torch.cuda.Stream()
+    assert _stream(None) == (torch.cuda.current_stream().cuda_stream or None)
+    with torch.cuda.stream(s):
+        assert _stream(None) == s.cuda_stream
+    assert _stream(s) == s.cuda_stream
