@@ -5,8 +5,8 @@
 // C_r = A_r @ B for every source r of the launch.  Persistent CTAs, one per
 // SM; the default kernel (mag2) runs them as CTA pairs (clusters of 2) that
 // compute 256 x 256 tiles with tcgen05.mma.cta_group::2, the 1-SM kernel
-// (mag1) 128 x 256 tiles.  Tiles are taken in column groups whose slice of B
-// stays in L2 (see tile_coord).  Per CTA:
+// (mag1) 128 x 256 tiles.  Tiles are taken in column groups, so that a wave
+// of tiles reads few distinct slices of A and B (see tile_coord).  Per CTA:
 //   * warp 0 (producer): TMA tensor loads of A (128 x 64, K-major) and of the
 //     CTA's columns of B (64-deep, N-major, 64-column boxes; one 3-d box per
 //     stage when N is a multiple of 64) into a ring of 128B-swizzled stages
@@ -412,10 +412,12 @@ struct TileCoord {
 };
 
 // Tile order: the tile columns are split into groups of a.tn_group; group by
-// group, every (source, tile row) runs over the group's columns.  A group's
-// slice of B stays in L2 while the tile rows stream past it (B would
-// otherwise be re-read from DRAM once per wave of tiles); A is read once per
-// group.
+// group, every (source, tile row) runs over the group's columns.  A wave of
+// concurrent tiles (one per CTA pair) then covers about (pairs / group)
+// tile rows and the group's columns, whose slices of A and B it reads from
+// DRAM once and shares through L2.  A is read once per group; the group's
+// slice of B, hinted evict_last, is nevertheless re-read about once per wave
+// on GB300 (measured with ncu), and groups of 7 at N=3584 read the least.
 __device__ __forceinline__ TileCoord tile_coord(const FusedArgs &a, int64_t t, int tiles_m,
                                                 int tiles_n)
 {
