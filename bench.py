@@ -858,166 +858,177 @@ def main():
     # ---- end to end through the C ABI, host buffers, copies in the timed region
     e2e = None
     if args.e2e_steps > 0:
-        if host is None:
-            # inputs were drawn on the device: stage them once into pinned host memory
-            def pinned_copy(t):
-                p = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                p.copy_(t)
-                return p
+        try:
+            if host is None:
+                # inputs were drawn on the device: stage them once into pinned host memory
+                def pinned_copy(t):
+                    p = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                    p.copy_(t)
+                    return p
 
-            pin = {"g_in": {}, "f_a": {}}
-            if g:
-                for h in g.members():
-                    pin["g_in"][h] = pinned_copy(sh.view(h, offs["g_in"], g_in_rows, g.N, g.N,
-                                                         gdt))
-            if f:
-                for h in f.members():
-                    pin["f_a"][h] = pinned_copy(sh.view(h, offs["f_a"], f.M, f.K, f.K, fdt))
-            pin_b = pinned_copy(Bd) if f else None
-        else:
-            pin = {k: {h: x.pin_memory() for h, x in v.items()} for k, v in host.items()
-                   if k != "B"}
-            pin_b = host["B"].pin_memory() if f else None
-        host = None
+                pin = {"g_in": {}, "f_a": {}}
+                if g:
+                    for h in g.members():
+                        pin["g_in"][h] = pinned_copy(sh.view(h, offs["g_in"], g_in_rows, g.N, g.N,
+                                                             gdt))
+                if f:
+                    for h in f.members():
+                        pin["f_a"][h] = pinned_copy(sh.view(h, offs["f_a"], f.M, f.K, f.K, fdt))
+                pin_b = pinned_copy(Bd) if f else None
+            else:
+                pin = {k: {h: x.pin_memory() for h, x in v.items()} for k, v in host.items()
+                       if k != "B"}
+                pin_b = host["B"].pin_memory() if f else None
+            host = None
 
-        # The step's result: the gathered outputs.  Every member holds an identical
-        # copy (what the parity tests check), so the result is read from the first
-        # member; the variant that reads all W copies is timed as well.
-        def out_set(members_g, members_f):
-            og = {h: torch.empty((g.W * g.M, g.N), dtype=gdt).pin_memory()
-                  for h in members_g}
-            of = {h: torch.empty((f.W * f.M, f.N), dtype=fdt).pin_memory()
-                  for h in members_f}
-            return og, of
+            # The step's result: the gathered outputs.  Every member holds an identical
+            # copy (what the parity tests check), so the result is read from the first
+            # member; the variant that reads all W copies is timed as well.
+            def out_set(members_g, members_f):
+                og = {h: torch.empty((g.W * g.M, g.N), dtype=gdt).pin_memory()
+                      for h in members_g}
+                of = {h: torch.empty((f.W * f.M, f.N), dtype=fdt).pin_memory()
+                      for h in members_f}
+                return og, of
 
-        first_g = g.members()[:1] if g else []
-        first_f = f.members()[:1] if f else []
-        outs = [out_set(first_g, first_f), out_set(first_g, first_f)]
-        h2d = sum(x.numel() * x.element_size() for v in pin.values() for x in v.values()) + \
-            (pin_b.numel() * 2 if f else 0)
+            first_g = g.members()[:1] if g else []
+            first_f = f.members()[:1] if f else []
+            outs = [out_set(first_g, first_f), out_set(first_g, first_f)]
+            h2d = sum(x.numel() * x.element_size() for v in pin.values() for x in v.values()) + \
+                (pin_b.numel() * 2 if f else 0)
 
-        def nbytes(oset):
-            return sum(x.numel() * x.element_size() for d in oset for x in d.values())
+            def nbytes(oset):
+                return sum(x.numel() * x.element_size() for d in oset for x in d.values())
 
-        d2h = nbytes(outs[0])
-        # every member's copy as well, while it fits a bounded pinned buffer
-        d2h_all = (g.W * g.W * g.M * g.N * g.es if g else 0) + \
-            (f.W * f.W * f.M * f.N * 2 if f else 0)
-        outs_all = ([out_set(g.members() if g else [], f.members() if f else [])] * 2
-                    if d2h_all <= E2E_ALL_COPIES_MAX_BYTES else None)
+            d2h = nbytes(outs[0])
+            # every member's copy as well, while it fits a bounded pinned buffer
+            d2h_all = (g.W * g.W * g.M * g.N * g.es if g else 0) + \
+                (f.W * f.W * f.M * f.N * 2 if f else 0)
+            outs_all = ([out_set(g.members() if g else [], f.members() if f else [])] * 2
+                        if d2h_all <= E2E_ALL_COPIES_MAX_BYTES else None)
 
-        def copy_in(heap, b_dev):
-            if g:
-                for h in g.members():
-                    heap.view(h, offs["g_in"], g_in_rows, g.N, g.N, gdt).copy_(pin["g_in"][h],
-                                                                                non_blocking=True)
-            if f:
-                for h in f.members():
-                    heap.view(h, offs["f_a"], f.M, f.K, f.K, fdt).copy_(pin["f_a"][h],
-                                                                         non_blocking=True)
-                b_dev.copy_(pin_b, non_blocking=True)
+            def copy_in(heap, b_dev):
+                if g:
+                    for h in g.members():
+                        heap.view(h, offs["g_in"], g_in_rows, g.N, g.N, gdt).copy_(pin["g_in"][h],
+                                                                                    non_blocking=True)
+                if f:
+                    for h in f.members():
+                        heap.view(h, offs["f_a"], f.M, f.K, f.K, fdt).copy_(pin["f_a"][h],
+                                                                             non_blocking=True)
+                    b_dev.copy_(pin_b, non_blocking=True)
 
-        def copy_out(heap, oset):
-            og, of = oset
-            for h, o in og.items():
-                o.copy_(heap.view(h, offs["g_out"], g.W * g.M, g.N, g.N, gdt), non_blocking=True)
-            for h, o in of.items():
-                o.copy_(heap.view(h, offs["f_out"], f.W * f.M, f.N, f.N, fdt), non_blocking=True)
+            def copy_out(heap, oset):
+                og, of = oset
+                for h, o in og.items():
+                    o.copy_(heap.view(h, offs["g_out"], g.W * g.M, g.N, g.N, gdt), non_blocking=True)
+                for h, o in of.items():
+                    o.copy_(heap.view(h, offs["f_out"], f.W * f.M, f.N, f.N, fdt), non_blocking=True)
 
-        e2e_steps = max(1, min(args.e2e_steps, args.steps))
+            e2e_steps = max(1, min(args.e2e_steps, args.steps))
 
-        # (1) serial: copy in, compute, copy out, one step after the other, one stream
-        def serial_step():
-            copy_in(sh, Bd)
-            launch_step(sh, Bd, stream)
-            copy_out(sh, outs[0])
+            # (1) serial: copy in, compute, copy out, one step after the other, one stream
+            def serial_step():
+                copy_in(sh, Bd)
+                launch_step(sh, Bd, stream)
+                copy_out(sh, outs[0])
 
-        for _ in range(3):
-            serial_step()
-        barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            serial_step()
-        e1.record(stream)
-        barrier()
-        serial_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
-
-        # (2) pipelined: two device buffer sets; step i copies in on one stream,
-        # computes on another and copies out on a third, overlapping steps i-1
-        # and i+1 (every step still moves all of its inputs and outputs)
-        sh2 = gg.SymmetricHeap(sh.H, sh.part_bytes, device=dev)
-        bufs = [(sh, Bd), (sh2, torch.empty_like(Bd) if f else None)]
-        s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_cmp = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
-
-        run_kernels = [True]
-
-        def pipelined(n, out_sets):
-            for i in range(n):
-                b = i % 2
-                heap, b_dev = bufs[b]
-                with torch.cuda.stream(s_in):
-                    if i >= 2:
-                        s_in.wait_event(ev_cmp[b])  # step i-2 no longer reads these inputs
-                    copy_in(heap, b_dev)
-                    ev_in[b].record(s_in)
-                with torch.cuda.stream(s_cmp):
-                    s_cmp.wait_event(ev_in[b])
-                    if i >= 2:
-                        s_cmp.wait_event(ev_out[b])  # step i-2's outputs are copied out
-                    if run_kernels[0]:
-                        launch_step(heap, b_dev, s_cmp)
-                    ev_cmp[b].record(s_cmp)
-                with torch.cuda.stream(s_out):
-                    s_out.wait_event(ev_cmp[b])
-                    copy_out(heap, out_sets[b])
-                    ev_out[b].record(s_out)
-
-        def timed_pipeline(out_sets):
-            pipelined(3, out_sets)
+            for _ in range(3):
+                serial_step()
             barrier()
-            p0 = torch.cuda.Event(enable_timing=True)
-            p1 = torch.cuda.Event(enable_timing=True)
-            p0.record(s_in)
-            pipelined(e2e_steps, out_sets)
-            p1.record(s_out)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(e2e_steps):
+                serial_step()
+            e1.record(stream)
             barrier()
-            return max_over_ranks(p0.elapsed_time(p1) / e2e_steps, dev)
+            serial_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dev)
 
-        e2e_ms = timed_pipeline(outs)
-        # the same pipelined copies with no kernels: the host link's share of the step
-        run_kernels[0] = False
-        copies_ms = timed_pipeline(outs)
-        run_kernels[0] = True
-        if outs_all is not None:
-            all_copies = {"d2h_bytes_per_step": d2h_all, "ms_per_step": timed_pipeline(outs_all)}
-        else:
-            all_copies = {"d2h_bytes_per_step": d2h_all, "ms_per_step": None,
-                          "skipped": f"more than {E2E_ALL_COPIES_MAX_BYTES >> 30} GiB of pinned "
-                                     "host memory"}
-        e2e = {"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "steps": e2e_steps, "serial_ms_per_step": serial_ms,
-               "copies_only": {"ms_per_step": copies_ms,
-                               "GB/s": (h2d + d2h) / (copies_ms * 1e-3) / 1e9,
-                               "note": "the same pipelined host<->device copies with no kernels"},
-               "all_copies": all_copies,
-               "path": ("pinned host -> heap (cudaMemcpyAsync) -> C-ABI calls -> pinned host; "
-                        "every member's inputs copied in, the gathered outputs read back from "
-                        "member 0 (all members hold identical copies); steps pipelined over two "
-                        "device buffer sets and three streams; all_copies reads every member's "
-                        "output")}
-        del sh2, bufs
+            # (2) pipelined: two device buffer sets; step i copies in on one stream,
+            # computes on another and copies out on a third, overlapping steps i-1
+            # and i+1 (every step still moves all of its inputs and outputs)
+            sh2 = gg.SymmetricHeap(sh.H, sh.part_bytes, device=dev)
+            bufs = [(sh, Bd), (sh2, torch.empty_like(Bd) if f else None)]
+            s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+            ev_in = [torch.cuda.Event() for _ in range(2)]
+            ev_cmp = [torch.cuda.Event() for _ in range(2)]
+            ev_out = [torch.cuda.Event() for _ in range(2)]
+
+            run_kernels = [True]
+
+            def pipelined(n, out_sets):
+                for i in range(n):
+                    b = i % 2
+                    heap, b_dev = bufs[b]
+                    with torch.cuda.stream(s_in):
+                        if i >= 2:
+                            s_in.wait_event(ev_cmp[b])  # step i-2 no longer reads these inputs
+                        copy_in(heap, b_dev)
+                        ev_in[b].record(s_in)
+                    with torch.cuda.stream(s_cmp):
+                        s_cmp.wait_event(ev_in[b])
+                        if i >= 2:
+                            s_cmp.wait_event(ev_out[b])  # step i-2's outputs are copied out
+                        if run_kernels[0]:
+                            launch_step(heap, b_dev, s_cmp)
+                        ev_cmp[b].record(s_cmp)
+                    with torch.cuda.stream(s_out):
+                        s_out.wait_event(ev_cmp[b])
+                        copy_out(heap, out_sets[b])
+                        ev_out[b].record(s_out)
+
+            def timed_pipeline(out_sets):
+                pipelined(3, out_sets)
+                barrier()
+                p0 = torch.cuda.Event(enable_timing=True)
+                p1 = torch.cuda.Event(enable_timing=True)
+                p0.record(s_in)
+                pipelined(e2e_steps, out_sets)
+                p1.record(s_out)
+                barrier()
+                return max_over_ranks(p0.elapsed_time(p1) / e2e_steps, dev)
+
+            e2e_ms = timed_pipeline(outs)
+            # the same pipelined copies with no kernels: the host link's share of the step
+            run_kernels[0] = False
+            copies_ms = timed_pipeline(outs)
+            run_kernels[0] = True
+            if outs_all is not None:
+                all_copies = {"d2h_bytes_per_step": d2h_all, "ms_per_step": timed_pipeline(outs_all)}
+            else:
+                all_copies = {"d2h_bytes_per_step": d2h_all, "ms_per_step": None,
+                              "skipped": f"more than {E2E_ALL_COPIES_MAX_BYTES >> 30} GiB of pinned "
+                                         "host memory"}
+            e2e = {"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                   "steps": e2e_steps, "serial_ms_per_step": serial_ms,
+                   "copies_only": {"ms_per_step": copies_ms,
+                                   "GB/s": (h2d + d2h) / (copies_ms * 1e-3) / 1e9,
+                                   "note": "the same pipelined host<->device copies with no kernels"},
+                   "all_copies": all_copies,
+                   "path": ("pinned host -> heap (cudaMemcpyAsync) -> C-ABI calls -> pinned host; "
+                            "every member's inputs copied in, the gathered outputs read back from "
+                            "member 0 (all members hold identical copies); steps pipelined over two "
+                            "device buffer sets and three streams; all_copies reads every member's "
+                            "output")}
+            del sh2, bufs
+        except (RuntimeError, MemoryError) as exc:
+            # a failed end-to-end leg (e.g. pinned host memory exhausted) must not
+            # cost the device-timed line: report it instead (one process only;
+            # with replicas the other ranks would wait at the leg's barriers)
+            if world > 1:
+                raise
+            torch.cuda.synchronize(dev)
+            e2e = {"ms_per_step": None, "error": f"{type(exc).__name__}: {exc}"[:300]}
 
     # ---- roofline bookkeeping
     t_rg, t_rf = roofline_times(peaks, g, f)
     roof_step = t_rg + t_rf
     value = whole_job_value(roof_step, ms_step, world)
-    if e2e:
+    if e2e and e2e.get("ms_per_step"):
         e2e = {"value": whole_job_value(roof_step, e2e["ms_per_step"], world), "unit": UNIT, **e2e}
+    elif e2e:
+        e2e = {"value": None, "unit": UNIT, **e2e}
     hbm_peak = peaks["hbm_gbs"]
     tc_peak = peaks["bf16_tflops"] * F16_PER_BF16
     kernels = {}
