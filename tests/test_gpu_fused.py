@@ -107,6 +107,8 @@ INT_CASES = [
     (8, (0, 2, 4), 64, 512, 128, 3, 0, 0),        # strided subgroup, inactive heaps
     (8, (1, 2, 4), 129, 256, 64, 148, 0, 0),      # subgroup from heap 1, more CTAs than tiles
     (4, (0, 1, 4), 256, 768, 256, 1, 0, 0),       # one CTA walks 24 tiles (TMEM phases)
+    (8, (0, 1, 8), 256, 1024, 1024, 2, 0, 0),     # one pair walks 32 tiles at W=8: every
+                                                  # store slot of the paced epilogue
     (1, (0, 1, 1), 8, 8, 16, 1, 0, 0),            # tiny, W = 1
     (64, (0, 1, 64), 16, 256, 64, 40, 0, 0),      # 64 members: epilogue stores wrap the lanes
     (40, (3, 1, 33), 40, 264, 96, 400, 0, 8),     # 33 members from heap 3, more CTAs than SMs
