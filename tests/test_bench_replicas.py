@@ -48,3 +48,17 @@ def test_whole_job_value_sums_replicas():
     one = bench.whole_job_value(0.5e-3, 1.0, 1)
     assert one == pytest.approx(50.0)
     assert bench.whole_job_value(0.5e-3, 1.0, 4) == pytest.approx(4 * one)
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    """Under torchrun the reference arm (the oracle on the host cores) runs on
+    rank 0 alone; any other rank exits 0 at once without output."""
+    import bench
+    monkeypatch.setenv("RANK", "1")
+
+    class Args:
+        steps, warmup, gpus = 3, 3, 2
+
+    peaks, src = bench.load_peaks()
+    assert bench.run_reference(Args(), peaks, src, bench.GATHER, bench.FUSED) == 0
+    assert capsys.readouterr().out == ""
