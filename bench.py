@@ -81,7 +81,7 @@ class FusedCfg:
     programs: int = 0  # 0: one CTA per SM
     start: int = 0
     stride: int = 1
-    path: str = "auto"  # auto / 1sm / 2sm
+    path: str = "auto"  # auto / 1sm / 2sm / 2sm_wide
 
     def members(self):
         return [self.start + i * self.stride for i in range(self.W)]
@@ -1041,7 +1041,11 @@ def main():
                                  "traffic": traffic_for(kname, "ag_kernels.cu", g.describe())}
     if f:
         f_tfs = fused_flops(f) / (f_ms * 1e-3) / 1e12
-        fk = "mag1_kernel" if (f.path == "1sm" or f.programs < 2) else "mag2_kernel"
+        chosen = gg.matmul_all_gather_plan(sh.heap, -1, sh.ptr(f.start, offs["f_a"]), f.K, Bd, f.N,
+                                           sh.ptr(f.start, offs["f_out"]), f.N, f.M, f.N, f.K,
+                                           fdt, gg.FUSED_TILE, f.programs,
+                                           (f.start, f.stride, f.W), f.path)
+        fk = {"1sm": "mag1_kernel", "2sm": "mag2_kernel", "2sm_wide": "mag2w_kernel"}[chosen]
         kernels["matmul_all_gather"] = {"kernel": fk, "ms": f_ms, "TFLOP/s": f_tfs,
                                         "roofline_ms": 1e3 * t_rf, "frac": f_tfs / tc_peak,
                                         "bound": "tensor", "algorithmic_flops": fused_flops(f),

@@ -14,7 +14,7 @@ from dataclasses import dataclass
 import torch
 
 from ._lib import (GG_AG_AUTO, GG_AG_BULK, GG_AG_TMA, GG_AG_VECTOR, GG_BF16, GG_MAG_1SM, GG_MAG_2SM,
-                   GG_MAG_AUTO, GG_COLL_ALL_GATHER, GG_COLL_ALL_GATHER_PARTITIONED,
+                   GG_MAG_2SM_WIDE, GG_MAG_AUTO, GG_COLL_ALL_GATHER, GG_COLL_ALL_GATHER_PARTITIONED,
                    GG_COLL_ALL_TO_ALL, GG_ERR_ALIGNMENT,
                    GG_ERR_CUDA, GG_ERR_INVALID_ARG, GG_ERR_NOT_IN_HEAP, GG_ERR_TIMEOUT,
                    GG_ERR_UNSUPPORTED, GG_F16, GG_F32, GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N,
@@ -26,7 +26,8 @@ __all__ = [
     "heap_create", "heap_wrap", "heap_bases", "heap_info", "heap_destroy", "heap_set_workspace",
     "all_gather", "all_gather_noalloc",
     "all_gather_check", "all_gather_grouped", "all_gather_partitioned", "all_to_all",
-    "collective_check", "matmul_all_gather", "matmul_all_gather_check", "set_claim_policy",
+    "collective_check", "matmul_all_gather", "matmul_all_gather_check", "matmul_all_gather_plan",
+    "set_claim_policy",
     "get_claim_policy", "CLAIM_POLICIES", "set_wait_limit_ns",
     "get_wait_limit_ns", "debug_inject_stall", "device_status", "clear_device_status",
     "SymmetricHeap", "Heap", "GGError", "DTYPE_CODES", "PATHS",
@@ -35,7 +36,8 @@ __all__ = [
 
 DTYPE_CODES = {torch.float16: GG_F16, torch.bfloat16: GG_BF16, torch.float32: GG_F32}
 PATHS = {"auto": GG_AG_AUTO, "bulk": GG_AG_BULK, "vector": GG_AG_VECTOR, "tma": GG_AG_TMA}
-FUSED_PATHS = {"auto": GG_MAG_AUTO, "1sm": GG_MAG_1SM, "2sm": GG_MAG_2SM}
+FUSED_PATHS = {"auto": GG_MAG_AUTO, "1sm": GG_MAG_1SM, "2sm": GG_MAG_2SM,
+               "2sm_wide": GG_MAG_2SM_WIDE}
 FUSED_TILE = (GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N)
 CLAIM_POLICIES = {"auto": GG_CLAIM_AUTO, "always": GG_CLAIM_ALWAYS, "never": GG_CLAIM_NEVER}
 
@@ -221,6 +223,21 @@ def matmul_all_gather_check(heap: Heap, rank: int, A, lda: int, B, ldb: int, out
     check(lib.gg_matmul_all_gather_check(heap.handle, rank, _ptr(A), lda, _ptr(B), ldb,
                                          _ptr(output), ld_out, M, N, K, _dtype(dtype),
                                          Tile(*tile), comm_programs, Group(*group)))
+
+
+def matmul_all_gather_plan(heap: Heap, rank: int, A, lda: int, B, ldb: int, output, ld_out: int,
+                           M: int, N: int, K: int, dtype, tile: tuple[int, int],
+                           comm_programs: int, group: tuple[int, int, int],
+                           path: str = "auto") -> str:
+    """Validate without launching; returns the kernel a launch would run
+    ("1sm", "2sm", "2sm_wide"; "none" when there is nothing to launch)."""
+    chosen = ctypes.c_int()
+    check(lib.gg_matmul_all_gather_plan(heap.handle, rank, _ptr(A), lda, _ptr(B), ldb,
+                                        _ptr(output), ld_out, M, N, K, _dtype(dtype), Tile(*tile),
+                                        comm_programs, Group(*group), FUSED_PATHS[path],
+                                        ctypes.byref(chosen)))
+    return {GG_MAG_AUTO: "none", GG_MAG_1SM: "1sm", GG_MAG_2SM: "2sm",
+            GG_MAG_2SM_WIDE: "2sm_wide"}[chosen.value]
 
 
 def set_claim_policy(policy: str) -> None:

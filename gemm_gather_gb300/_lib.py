@@ -21,7 +21,7 @@ GG_ERR_TIMEOUT = -6
 
 GG_F16, GG_BF16, GG_F32 = 0, 1, 2
 GG_AG_AUTO, GG_AG_BULK, GG_AG_VECTOR, GG_AG_TMA = 0, 1, 2, 3
-GG_MAG_AUTO, GG_MAG_1SM, GG_MAG_2SM = 0, 1, 2
+GG_MAG_AUTO, GG_MAG_1SM, GG_MAG_2SM, GG_MAG_2SM_WIDE = 0, 1, 2, 3
 GG_COLL_ALL_GATHER, GG_COLL_ALL_GATHER_PARTITIONED, GG_COLL_ALL_TO_ALL = 0, 1, 2
 GG_MAX_WORLD = 64
 GG_MAX_HEAPS = 1024
@@ -37,6 +37,7 @@ EXPORTS = (
     "gg_all_gather_grouped",
     "gg_all_gather_partitioned", "gg_all_to_all", "gg_collective_check",
     "gg_matmul_all_gather", "gg_matmul_all_gather_path", "gg_matmul_all_gather_check",
+    "gg_matmul_all_gather_plan",
     "gg_set_claim_policy", "gg_get_claim_policy",
     "gg_set_wait_limit_ns", "gg_get_wait_limit_ns", "gg_debug_inject_stall",
     "gg_device_status", "gg_clear_device_status",
@@ -86,6 +87,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
                                        Tile, i32, Group, vp, vp, i32], i32),
         "gg_matmul_all_gather_check": ([vp, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, i32,
                                         Tile, i32, Group], i32),
+        "gg_matmul_all_gather_plan": ([vp, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, i32,
+                                       Tile, i32, Group, i32, ctypes.POINTER(i32)], i32),
         "gg_set_claim_policy": ([i32], i32),
         "gg_get_claim_policy": ([], i32),
         "gg_set_wait_limit_ns": ([u64], i32),

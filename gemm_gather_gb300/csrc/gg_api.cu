@@ -724,10 +724,11 @@ gg_status gg_matmul_all_gather_path(const gg_heap *heap, int rank, const void *A
                                     int comm_programs, gg_group group, int *dev_status,
                                     gg_stream_t stream, gg_mag_path path)
 {
-    if (path != GG_MAG_AUTO && path != GG_MAG_1SM && path != GG_MAG_2SM)
+    if (path != GG_MAG_AUTO && path != GG_MAG_1SM && path != GG_MAG_2SM &&
+        path != GG_MAG_2SM_WIDE)
         return fail(GG_ERR_INVALID_ARG, "unknown fused path %d", (int)path);
-    if (path == GG_MAG_2SM && comm_programs < 2)
-        return fail(GG_ERR_INVALID_ARG, "the 2-SM path needs comm_programs >= 2 (one CTA pair)");
+    if ((path == GG_MAG_2SM || path == GG_MAG_2SM_WIDE) && comm_programs < 2)
+        return fail(GG_ERR_INVALID_ARG, "the 2-SM paths need comm_programs >= 2 (one CTA pair)");
     gg::FusedArgs f;
     static thread_local gg::OutMaps maps;
     bool launch = false;
@@ -766,6 +767,28 @@ gg_status gg_matmul_all_gather_check(const gg_heap *heap, int rank, const void *
     bool launch = false;
     return prepare_fused(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype, tile,
                          comm_programs, group, nullptr, &f, nullptr, &launch);
+}
+
+gg_status gg_matmul_all_gather_plan(const gg_heap *heap, int rank, const void *A, int64_t lda,
+                                    const void *B, int64_t ldb, void *output, int64_t ld_out,
+                                    int64_t M, int64_t N, int64_t K, gg_dtype dtype, gg_tile tile,
+                                    int comm_programs, gg_group group, gg_mag_path path,
+                                    gg_mag_path *chosen)
+{
+    if (chosen)
+        *chosen = GG_MAG_AUTO;
+    if (path != GG_MAG_AUTO && path != GG_MAG_1SM && path != GG_MAG_2SM &&
+        path != GG_MAG_2SM_WIDE)
+        return fail(GG_ERR_INVALID_ARG, "unknown fused path %d", (int)path);
+    if ((path == GG_MAG_2SM || path == GG_MAG_2SM_WIDE) && comm_programs < 2)
+        return fail(GG_ERR_INVALID_ARG, "the 2-SM paths need comm_programs >= 2 (one CTA pair)");
+    gg::FusedArgs f;
+    bool launch = false;
+    gg_status st = prepare_fused(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype, tile,
+                                 comm_programs, group, nullptr, &f, nullptr, &launch);
+    if (st == GG_OK && launch && chosen)
+        *chosen = (gg_mag_path)gg::fused_variant(N, comm_programs, (int)path);
+    return st;
 }
 
 gg_status gg_set_wait_limit_ns(uint64_t ns)

@@ -101,7 +101,23 @@ struct FusedArgs {
     int tn_group;      // set by the launcher: tile columns per group of the tile order
 };
 
-// variant: 0 = automatic (2-SM pairs when programs >= 2), 1 = 1-SM, 2 = 2-SM
+// Fused kernel variants: 1 = 1-SM 128 x 256 tiles, 2 = 2-SM 256 x 256 pair
+// tiles, 3 = 2-SM 256 x 512 pair tiles; 0 = automatic.
+// The variant a launch runs for `requested` (0..3): one CTA runs the 1-SM
+// kernel; the automatic choice takes 256 x 512 pair tiles unless they pad N
+// by more than 1/16 beyond what 256-column tiles pad, else 256 x 256.
+inline int fused_variant(int64_t N, int programs, int requested)
+{
+    if (requested == 1 || programs < 2)
+        return 1;
+    if (requested == 2 || requested == 3)
+        return requested;
+    const int64_t cols_narrow = (N + 255) / 256 * 256;
+    const int64_t cols_wide = (N + 511) / 512 * 512;
+    return 16 * cols_wide <= 17 * cols_narrow ? 3 : 2;
+}
+
+// variant: 0 = automatic, 1 / 2 / 3 as fused_variant
 cudaError_t launch_matmul_all_gather(const FusedArgs &a, const OutMaps &out, int programs,
                                      int variant, cudaStream_t s, const char **why);
 

@@ -54,8 +54,11 @@ constexpr int kMaxStages = 8;
 // 2-d box per 64 columns: one TMA instruction fewer per stage (measured
 // +0-2.5%).
 constexpr bool kBBoxes3d = true;
-// Bytes of B one column group of the tile order may span (see tile_coord).
+// Bytes of B one column group of the tile order may span (see tile_coord):
+// 256-column tiles / 512-column tiles (measured best at N=3584, K=8192:
+// groups of 7 narrow tiles, one group of 7 wide ones).
 constexpr int64_t kBGroupBytes = 32ll << 20;
+constexpr int64_t kBGroupBytesWide = 64ll << 20;
 constexpr int kKAtom = 64;                      // K elements of one 128-byte swizzle row
 constexpr int kAAtom = BM * kKAtom * 2;         // 16 KB: 128 rows x 64 K, K-major
 constexpr int kThreads = 192;                   // 6 warps
@@ -332,6 +335,27 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
         : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld16(uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
 }
 
 // Wait for this thread's tcgen05.ld to complete.  The loaded registers are
@@ -781,6 +805,320 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mag_body<2>(map_a, map_b, out, a);
 }
 
+// ---- wide pair tiles: 256 x 512 per CTA pair ------------------------------------
+// The same pipeline with two N=256 MMAs per K step, side by side, sharing the
+// A stage: a stage (A 16 KB + this CTA's 256 columns of B, 32 KB) feeds twice
+// the tensor work of a 256 x 256 stage, so the 4-stage ring holds about a
+// third more tensor time in flight.  The accumulator takes all 512 TMEM
+// columns; eight epilogue warps (two per TMEM lane quarter, 256 columns each)
+// copy it into registers as packed f16/bf16 right after the tile's last MMA
+// and release it, then store from registers through one staged box per warp.
+namespace wide {
+constexpr int kStages = 4;
+constexpr int kBK = 64;                          // one 128-byte swizzle atom of A
+constexpr int kAStage = BM * kBK * 2;            // 16 KB
+constexpr int kBBox = kBK * 64 * 2;              // 8 KB: 64 K-rows x 64 columns
+constexpr int kBHalf = 2 * kBBox;                // this CTA's 128 columns of one N half
+constexpr int kBStage = 2 * kBHalf;              // both N halves: 32 KB
+constexpr int kTileM = 2 * BM;                   // 256 rows per pair tile
+constexpr int kTileN = 2 * BN;                   // 512 columns per pair tile
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;    // producer, MMA, 8 epilogue warps
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kStages * kAStage;
+constexpr int kOffEpi = kOffB + kStages * kBStage;
+constexpr int kOffShared = kOffEpi + kEpiWarps * kBox;
+constexpr int kSmemBytes = kOffShared + (int)sizeof(FusedShared) + 1024;
+static_assert(kSmemBytes <= 232448, "at most 227 KB of dynamic shared memory per CTA");
+static_assert(kStages <= kMaxStages, "ring barriers");
+}  // namespace wide
+
+__device__ __forceinline__ void magw_body(const CUtensorMap &map_a, const CUtensorMap &map_b,
+                                          const OutMaps &out, const FusedArgs &a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-aligned for the 128B swizzle
+    uint8_t *smem = smem_raw + (base - raw);
+    FusedShared &sh = *reinterpret_cast<FusedShared *>(smem + wide::kOffShared);
+    volatile int *abort_flag = &sh.abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int64_t unit = (int64_t)cluster_id_x();
+    const int64_t nunits = (int64_t)ncluster_x();
+    const int tiles_m = (int)((a.M + wide::kTileM - 1) / wide::kTileM);
+    const int tiles_n = (int)((a.N + wide::kTileN - 1) / wide::kTileN);
+    const int64_t total = (int64_t)a.n_src * tiles_m * tiles_n;
+    const int num_kb = (int)((a.K + wide::kBK - 1) / wide::kBK);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < wide::kStages; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&sh.full[s]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sh.empty[s]), 1);
+        }
+        ptx::mbar_init(ptx::smem_addr(&sh.tmem_full[0]), 1);
+        ptx::mbar_init(ptx::smem_addr(&sh.tmem_empty[0]), 2 * wide::kEpiWarps);
+        ptx::mbar_init(ptx::smem_addr(&sh.mma_done), 1);
+        sh.abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&map_a);
+        prefetch_tensormap(&map_b);
+    }
+    if (warp == 1) {
+        tmem_alloc<2>(ptx::smem_addr(&sh.tmem_base));
+        tc_fence_before();
+    }
+    if (threadIdx.x < (unsigned)a.W)
+        prefetch_tensormap(&out.map[threadIdx.x]);
+    __syncthreads();
+    cluster_sync();  // the peer's barriers exist before anything signals them
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+
+    if (warp == 0) {
+        // ===================== producer =====================================
+        const uint64_t pol_a = ptx::policy_evict_normal();
+        const uint64_t pol_b = ptx::policy_evict_last();
+        constexpr uint32_t kTx = 2 * (wide::kAStage + wide::kBStage);  // both CTAs
+        int stage = 0;
+        uint32_t phase = 0;
+        int64_t issued = 0;
+        bool ok = true;
+        for (int64_t t = unit; t < total && ok; t += nunits) {
+            const TileCoord c = tile_coord(a, t, tiles_m, tiles_n);
+            const int h_coord = a.a_abs ? 0 : c.h;
+            const int row0 = c.tm * wide::kTileM + (int)rank * BM;
+            const int colh0 = c.tn * wide::kTileN + (int)rank * (BN / 2);  // N half 0
+            for (int kq = 0; kq < num_kb; ++kq) {
+                const bool got = role_wait(ptx::smem_addr(&sh.empty[stage]), phase ^ 1u,
+                                           a.wait_limit_ns, abort_flag);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                const bool stall = a.inject_stall && unit == 0 && issued == 0;
+                if (lane == 0 && !stall) {  // test hook: the first stage is never armed
+                    const uint32_t local_full = ptx::smem_addr(&sh.full[stage]);
+                    const uint32_t bar = map_to_rank(local_full, 0);
+                    if (leader)
+                        ptx::mbar_arrive_expect_tx(local_full, kTx);
+                    const uint32_t sa = base + wide::kOffA + stage * wide::kAStage;
+                    const uint32_t sb = base + wide::kOffB + stage * wide::kBStage;
+                    tma_load_3d<2>(sa, &map_a, kq * wide::kBK, row0, h_coord, bar, pol_a);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int col0 = colh0 + h * BN;
+                        if (a.b_boxes3d) {
+                            tma_load_3d<2>(sb + h * wide::kBHalf, &map_b, 0, kq * wide::kBK,
+                                           col0 / 64, bar, pol_b);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 2; ++j)
+                                tma_load_2d<2>(sb + h * wide::kBHalf + j * wide::kBBox, &map_b,
+                                               col0 + j * 64, kq * wide::kBK, bar, pol_b);
+                        }
+                    }
+                }
+                __syncwarp();
+                ++issued;
+                if (++stage == wide::kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            report_status(a.status, kStatusTimeout);
+        }
+        if (leader) {
+            const int64_t pending = issued < wide::kStages ? issued : wide::kStages;
+            for (int64_t q = 0; q < pending; ++q) {
+                const int64_t idx = issued - 1 - q;
+                const int s = (int)(idx % wide::kStages);
+                const uint32_t ph = (uint32_t)((idx / wide::kStages) & 1);
+                ptx::mbar_wait(ptx::smem_addr(&sh.full[s]), ph, kDrainLimitNs);
+            }
+        } else if (!ok && issued > 0) {
+            sleep_ns(200000);
+        }
+    } else if (warp == 1) {
+        // ===================== MMA issuer (leader CTA) ======================
+        const uint32_t idesc = instr_desc(a.is_bf16, 2);
+        int stage = 0;
+        uint32_t phase = 0;
+        int64_t lt = 0;
+        bool issued_any = false;
+        bool ok = true;
+        for (int64_t t = unit; leader && t < total && ok; t += nunits, ++lt) {
+            // the epilogue has copied the previous tile's accumulator out of TMEM
+            const bool free_acc = role_wait(ptx::smem_addr(&sh.tmem_empty[0]),
+                                            (uint32_t)(lt & 1) ^ 1u, a.wait_limit_ns, abort_flag);
+            if (!__all_sync(0xffffffffu, free_acc)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int kb = 0; kb < num_kb; ++kb) {
+                const bool got = role_wait(ptx::smem_addr(&sh.full[stage]), phase, a.wait_limit_ns,
+                                           abort_flag);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sa = base + wide::kOffA + stage * wide::kAStage;
+                    const uint32_t sb = base + wide::kOffB + stage * wide::kBStage;
+#pragma unroll
+                    for (int k = 0; k < wide::kBK / UK; ++k) {
+                        const uint64_t ad = smem_desc(sa + (uint32_t)(k * UK * 2), 16, 1024);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint64_t bd = smem_desc(
+                                sb + (uint32_t)(h * wide::kBHalf + k * (UK * 128)), wide::kBBox, 1024);
+                            mma_f16<2>(tmem + (uint32_t)(h * BN), ad, bd, idesc,
+                                       (kb | k) != 0 ? 1u : 0u);
+                        }
+                    }
+                    mma_commit_all<2>(ptx::smem_addr(&sh.empty[stage]));
+                }
+                __syncwarp();
+                issued_any = true;
+                if (++stage == wide::kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok)
+                break;
+            if (lane == 0)
+                mma_commit_all<2>(ptx::smem_addr(&sh.tmem_full[0]));
+            __syncwarp();
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            report_status(a.status, kStatusTimeout);
+        }
+        if (issued_any) {
+            if (lane == 0)
+                mma_commit_local<2>(ptx::smem_addr(&sh.mma_done));
+            __syncwarp();
+            ptx::mbar_wait(ptx::smem_addr(&sh.mma_done), 0, kDrainLimitNs);
+        }
+    } else {
+        // ===================== epilogue (warps 2-9) =========================
+        const int ew = warp - 2;                   // 0..7
+        const int q = warp & 3;                    // TMEM lane quarter this warp may access
+        const int half = ew >> 2;                  // columns [half*256, half*256 + 256)
+        const uint32_t staging = base + wide::kOffEpi + (uint32_t)(ew * kBox);
+        const uint32_t my_row = staging + (uint32_t)lane * 128u;  // row `lane` of the box
+        const uint32_t swz = (uint32_t)(lane & 7);
+        const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(half * BN);
+        const uint64_t pol_c = ptx::policy_evict_first();
+        constexpr int kBoxes = BN / 64;            // 4 boxes of 64 columns per warp and tile
+        int64_t lt = 0;
+        bool ok = true;
+        uint64_t prev_ready = ptx::globaltimer();
+        for (int64_t t = unit; t < total; t += nunits, ++lt) {
+            const TileCoord c = tile_coord(a, t, tiles_m, tiles_n);
+            const bool got = role_wait(ptx::smem_addr(&sh.tmem_full[0]), (uint32_t)(lt & 1),
+                                       a.wait_limit_ns, abort_flag);
+            if (!__all_sync(0xffffffffu, got)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t t_ready = ptx::globaltimer();
+            uint64_t period = t_ready - prev_ready;
+            period = period > kPaceMaxPeriodNs ? kPaceMaxPeriodNs : period;
+            prev_ready = t_ready;
+            const uint64_t slot =
+                t + nunits < total ? period * kPacePct / 100u / (uint64_t)(kBoxes * a.W) : 0;
+            // the whole accumulator slice of this warp, as packed 16-bit pairs
+            // (16 columns per load keeps it within the registers, no spills)
+            uint32_t pk[kBoxes * 32];
+#pragma unroll
+            for (int ch = 0; ch < 4 * kBoxes; ++ch) {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(t_lane + (uint32_t)(ch * 16), v);
+                tmem_wait_ld16(v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    pk[ch * 8 + i] = pack2(v[2 * i], v[2 * i + 1], a.is_bf16);
+            }
+            // accumulator copied out: hand TMEM back to the leader's MMA warp
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(map_to_rank(ptx::smem_addr(&sh.tmem_empty[0]), 0));
+            const int row0 = c.tm * wide::kTileM + (int)rank * BM + q * 32;
+#pragma unroll
+            for (int b = 0; b < kBoxes; ++b) {
+                // the box is free once this warp's previous stores have read it
+                ptx::bulk_wait_read<0>();
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k)  // 16-byte chunk k at position k ^ (row mod 8)
+                    st_shared_v4(my_row + ((((uint32_t)k) ^ swz) << 4), pk[b * 32 + 4 * k],
+                                 pk[b * 32 + 4 * k + 1], pk[b * 32 + 4 * k + 2],
+                                 pk[b * 32 + 4 * k + 3]);
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                const int col = c.tn * wide::kTileN + half * BN + b * 64;
+                if (row0 < a.M && col < a.N) {
+                    if (slot != 0) {
+                        for (int j = 0; j < a.W; ++j) {
+                            const uint64_t due = t_ready + slot * (uint64_t)(b * a.W + j);
+                            while (ptx::globaltimer() < due && !*abort_flag)
+                                __nanosleep(256);
+                            if (lane == 0) {
+                                int i = c.g + j;
+                                if (i >= a.W)
+                                    i -= a.W;
+                                tma_store_3d(&out.map[i], staging, col, row0, c.g, pol_c);
+                            }
+                        }
+                    } else {
+                        for (int j = lane; j < a.W; j += 32) {
+                            int i = c.g + j;
+                            if (i >= a.W)
+                                i -= a.W;
+                            tma_store_3d(&out.map[i], staging, col, row0, c.g, pol_c);
+                        }
+                    }
+                }
+                ptx::bulk_commit();
+            }
+        }
+        if (!ok) {
+            *abort_flag = 1;
+            report_status(a.status, kStatusTimeout);
+        }
+        ptx::bulk_wait_all();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the leader's MMAs into the peer's TMEM and smem are done
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc<2>(tmem);
+    }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(wide::kThreads, 1)
+    mag2w_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                 const __grid_constant__ OutMaps out, const FusedArgs a)
+{
+    magw_body(map_a, map_b, out, a);
+}
+
 }  // namespace
 
 cudaError_t launch_matmul_all_gather(const FusedArgs &a, const OutMaps &out, int programs,
@@ -808,16 +1146,19 @@ cudaError_t launch_matmul_all_gather(const FusedArgs &a, const OutMaps &out, int
             return cudaErrorInvalidValue;
         }
     }
-    const bool two_sm = variant != 1 && programs >= 2;
+    const int chosen = fused_variant(a.N, programs, variant);
+    const bool two_sm = chosen != 1;
+    const bool wide_tiles = chosen == 3;  // 256 x 512 pair tiles
     const int bk = two_sm ? Geo<2>::kBK : Geo<1>::kBK;  // K rows of one B box
     FusedArgs args = a;
     args.b_boxes3d = 0;
     {
-        // column groups whose B slice (K x 256 columns each) fits in
+        // column groups whose B slice (K x the tile's columns each) fits in
         // kBGroupBytes, as equal as possible
-        const int64_t tn = a.N > BN ? (a.N + BN - 1) / BN : 1;
-        const int64_t per_col = a.K * BN * 2;
-        int64_t w = kBGroupBytes / (per_col > 0 ? per_col : 1);
+        const int64_t tile_n = wide_tiles ? wide::kTileN : BN;
+        const int64_t tn = a.N > tile_n ? (a.N + tile_n - 1) / tile_n : 1;
+        const int64_t per_col = a.K * tile_n * 2;
+        int64_t w = (wide_tiles ? kBGroupBytesWide : kBGroupBytes) / (per_col > 0 ? per_col : 1);
         w = w < 1 ? 1 : (w > tn ? tn : w);
         const int64_t groups = (tn + w - 1) / w;
         args.tn_group = (int)((tn + groups - 1) / groups);
@@ -844,7 +1185,45 @@ cudaError_t launch_matmul_all_gather(const FusedArgs &a, const OutMaps &out, int
     }
     const int64_t tiles_n = (a.N + BN - 1) / BN;
     cudaError_t e;
-    if (two_sm) {
+    if (wide_tiles) {
+        const int64_t pairs = (int64_t)a.n_src * ((a.M + wide::kTileM - 1) / wide::kTileM) *
+                              ((a.N + wide::kTileN - 1) / wide::kTileN);
+        e = cudaFuncSetAttribute(mag2w_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 wide::kSmemBytes);
+        if (e != cudaSuccess) {
+            *why = "setting the shared-memory size of the fused kernel";
+            return e;
+        }
+        static int resident_by_dev[64];
+        static std::once_flag once_by_dev[64];
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+            dev = 0;
+        std::call_once(once_by_dev[dev], [&] {
+            int resident = 0;
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(2, 1, 1);
+            cfg.blockDim = dim3(wide::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = wide::kSmemBytes;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&resident, mag2w_kernel, &cfg) != cudaSuccess)
+                resident = 0;
+            (void)cudaGetLastError();
+            resident_by_dev[dev] = resident;
+        });
+        const int resident = resident_by_dev[dev];
+        int64_t clusters = gg_min64(programs / 2, pairs);
+        if (resident > 0)
+            clusters = gg_min64(clusters, resident);
+        mag2w_kernel<<<(int)(2 * clusters), wide::kThreads, wide::kSmemBytes, s>>>(map_a, map_b,
+                                                                                 out, args);
+    } else if (two_sm) {
         const int64_t pairs = (int64_t)a.n_src * ((a.M + 2 * BM - 1) / (2 * BM)) * tiles_n;
         e = cudaFuncSetAttribute(mag2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  smem_bytes<2>());

@@ -329,8 +329,8 @@ gg_status gg_collective_check(gg_collective kind, const gg_heap *heap, int rank,
  *   lda, ldb, ld_out multiples of 8; N a multiple of 8.
  * comm_programs: number of persistent CTAs (one per SM at most is useful).
  *   By default they run as CTA pairs (comm_programs/2 clusters of two CTAs,
- *   a 256 x 256 output tile per pair); a single program runs alone on
- *   128 x 256 tiles.
+ *   a 256 x 512 output tile per pair, or 256 x 256 where that pads N
+ *   noticeably less); a single program runs alone on 128 x 256 tiles.
  * dev_status: as for gg_all_gather (NULL: the library's status word).
  * M, N or K == 0: nothing is launched, GG_OK (with K == 0 nothing is
  *   written either).
@@ -342,17 +342,39 @@ gg_status gg_matmul_all_gather(const gg_heap *heap, int rank, const void *A, int
                                int *dev_status, gg_stream_t stream);
 
 /* Kernel variants of gg_matmul_all_gather (same arguments and result):
- *   GG_MAG_AUTO  2-SM pairs when comm_programs >= 2, else 1-SM
- *   GG_MAG_1SM   one CTA per 128 x 256 tile (tcgen05.mma.cta_group::1)
- *   GG_MAG_2SM   a CTA pair per 256 x 256 tile (tcgen05.mma.cta_group::2);
- *                needs comm_programs >= 2 (else GG_ERR_INVALID_ARG) */
-typedef enum { GG_MAG_AUTO = 0, GG_MAG_1SM = 1, GG_MAG_2SM = 2 } gg_mag_path;
+ *   GG_MAG_AUTO       2-SM pairs when comm_programs >= 2 (256 x 512 tiles
+ *                     unless they pad N noticeably more, see
+ *                     gg_matmul_all_gather_plan), else 1-SM
+ *   GG_MAG_1SM        one CTA per 128 x 256 tile (tcgen05.mma.cta_group::1)
+ *   GG_MAG_2SM        a CTA pair per 256 x 256 tile (tcgen05.mma.cta_group::2);
+ *                     needs comm_programs >= 2 (else GG_ERR_INVALID_ARG)
+ *   GG_MAG_2SM_WIDE   a CTA pair per 256 x 512 tile: two MMAs share each A
+ *                     stage; needs comm_programs >= 2 */
+typedef enum {
+    GG_MAG_AUTO = 0,
+    GG_MAG_1SM = 1,
+    GG_MAG_2SM = 2,
+    GG_MAG_2SM_WIDE = 3
+} gg_mag_path;
 
 gg_status gg_matmul_all_gather_path(const gg_heap *heap, int rank, const void *A, int64_t lda,
                                     const void *B, int64_t ldb, void *output, int64_t ld_out,
                                     int64_t M, int64_t N, int64_t K, gg_dtype dtype, gg_tile tile,
                                     int comm_programs, gg_group group, int *dev_status,
                                     gg_stream_t stream, gg_mag_path path);
+
+/* Validate a gg_matmul_all_gather_path call exactly as the launching call
+ * does and launch nothing; *chosen (nullable) receives the kernel a launch
+ * would run: GG_MAG_1SM (a single program, or asked for), GG_MAG_2SM or
+ * GG_MAG_2SM_WIDE.  For GG_MAG_AUTO with comm_programs >= 2 that is the wide
+ * 256 x 512 pair tile unless it pads N by more than 1/16 beyond what
+ * 256-column tiles pad (N = 256: GG_MAG_2SM; N = 3584: GG_MAG_2SM_WIDE).
+ * GG_MAG_AUTO when there is nothing to launch. */
+gg_status gg_matmul_all_gather_plan(const gg_heap *heap, int rank, const void *A, int64_t lda,
+                                    const void *B, int64_t ldb, void *output, int64_t ld_out,
+                                    int64_t M, int64_t N, int64_t K, gg_dtype dtype,
+                                    gg_tile tile, int comm_programs, gg_group group,
+                                    gg_mag_path path, gg_mag_path *chosen);
 
 /* Validate a gg_matmul_all_gather call exactly as the launching call does
  * and launch nothing. */

@@ -173,6 +173,42 @@ def mag(heap, **kw):
                                a["comm_programs"], a["group"])
 
 
+def plan(heap, path="auto", **kw):
+    a = dict(rank=-1, A=BASE + 4096, lda=1024, B=TABLE + 4096, ldb=8192, output=BASE + (4 << 20),
+             ld_out=8192, M=64, N=512, K=1024, dtype=torch.float16, tile=gg.FUSED_TILE,
+             comm_programs=148, group=(0, 1, 4))
+    a.update(kw)
+    return gg.matmul_all_gather_plan(heap, a["rank"], a["A"], a["lda"], a["B"], a["ldb"],
+                                     a["output"], a["ld_out"], a["M"], a["N"], a["K"], a["dtype"],
+                                     a["tile"], a["comm_programs"], a["group"], path)
+
+
+@pytest.mark.parametrize("N,want", [
+    (512, "2sm_wide"), (3584, "2sm_wide"), (264, "2sm_wide"),   # same padding either way
+    (256, "2sm"), (8, "2sm"), (768, "2sm"), (1280, "2sm"),       # 256-column tiles pad less
+    (4352, "2sm_wide"),                                           # 17 x 256: 1/16 more padding
+    (2304, "2sm"),                                                # 9 x 256: 1/9 more padding
+])
+def test_fused_plan_automatic_choice(heap, N, want):
+    """The automatic fused path takes 256 x 512 pair tiles unless they pad N
+    by more than 1/16 beyond what 256-column tiles pad."""
+    assert plan(heap, N=N) == want
+
+
+def test_fused_plan_explicit_paths(heap):
+    assert plan(heap, comm_programs=1) == "1sm"
+    assert plan(heap, path="1sm") == "1sm"
+    assert plan(heap, path="2sm") == "2sm"
+    assert plan(heap, path="2sm_wide", N=256) == "2sm_wide"
+    assert plan(heap, M=0) == "none"
+    with pytest.raises(gg.GGError) as e:
+        plan(heap, path="2sm_wide", comm_programs=1)
+    assert e.value.status == _lib.GG_ERR_INVALID_ARG
+    with pytest.raises(gg.GGError) as e:
+        plan(heap, tile=(256, 128))
+    assert e.value.status == _lib.GG_ERR_UNSUPPORTED
+
+
 def test_fused_valid_calls(heap):
     mag(heap)
     mag(heap, rank=2, A=TABLE + (1 << 20))

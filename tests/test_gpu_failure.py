@@ -63,7 +63,7 @@ def test_gather_wait_limit_reports_timeout(oracle, short_waits, path):
     assert np.array_equal(got, host), first_diff(got, host, lay)
 
 
-@pytest.mark.parametrize("path", ["1sm", "2sm"])
+@pytest.mark.parametrize("path", ["1sm", "2sm", "2sm_wide"])
 def test_fused_wait_limit_reports_timeout(oracle, short_waits, path):
     import gemm_gather_gb300 as gg
     W, M, N, K = 2, 512, 1024, 2048
@@ -98,14 +98,14 @@ def test_fused_wait_limit_reports_timeout(oracle, short_waits, path):
     assert np.array_equal(got, host), first_diff(got, host, lay)
 
 
-@pytest.mark.parametrize("kind", ["bulk", "tma", "1sm", "2sm"])
+@pytest.mark.parametrize("kind", ["bulk", "tma", "1sm", "2sm", "2sm_wide"])
 def test_timeout_without_status_word_is_reported(oracle, short_waits, kind):
     """A launch given no status word (NULL) reports a wait that gave up in the
     library's status word of the device: no early stop goes unreported.  After
     clearing it, the same launch runs normally, leaves the word at 0 and gives
     the oracle's heap."""
     import gemm_gather_gb300 as gg
-    fused = kind in ("1sm", "2sm")
+    fused = kind in ("1sm", "2sm", "2sm_wide")
     if fused:
         W, M, N, K = 2, 512, 1024, 2048
         lay = hi.make_layout(W, W, M, N, 2, ld_in=K)

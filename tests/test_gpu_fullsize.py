@@ -133,6 +133,7 @@ FUSED_CASES = [
     (8, (0, 1, 8), 1024, torch.float16, "auto"),
     (8, (0, 1, 8), 1024, torch.float16, "1sm"),
     (8, (0, 1, 8), 4096, torch.float16, "auto"),
+    (8, (0, 1, 8), 4096, torch.float16, "2sm"),       # the 256 x 256 pair kernel
     (8, (0, 1, 8), 4096, torch.bfloat16, "auto"),
     (8, (0, 1, 8), 16384, torch.float16, "auto"),
     (8, (0, 1, 8), 16384, torch.bfloat16, "auto"),

@@ -115,7 +115,7 @@ INT_CASES = [
 ]
 
 
-PATHS = ["1sm", "2sm"]
+PATHS = ["1sm", "2sm", "2sm_wide"]
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -123,7 +123,7 @@ PATHS = ["1sm", "2sm"]
 @pytest.mark.parametrize("case", INT_CASES, ids=lambda c: f"H{c[0]}g{c[1]}_{c[2]}x{c[3]}x{c[4]}p{c[5]}")
 def test_integer_operands_bit_exact(oracle, case, dtype, path):
     H, group, M, N, K, programs, lp, op = case
-    if path == "2sm" and programs < 2:
+    if path != "1sm" and programs < 2:
         programs = 2
     run_fused(oracle, H, group, M, N, K, dtype, programs, "int", lp, op, path=path)
 
