@@ -514,11 +514,12 @@ def sweep_points(name: str):
         for p in (8, 16, 32, 64, 148):  # W single-rank launches in turn
             pts.append((replace(GATHER, programs=p, kind="ranks"), None))
     elif name == "cublas":  # the fused kernel and cuBLAS on the plain GEMM of the same size
-        for M in (1024, 4096, 16384):
-            for dt in ("f16", "bf16"):
-                pts.append((None, replace(FUSED, M=M, dtype=dt, path="2sm")))
+        for path in ("auto", "2sm"):
+            for M in (1024, 4096, 16384):
+                for dt in ("f16", "bf16"):
+                    pts.append((None, replace(FUSED, M=M, dtype=dt, path=path)))
     elif name == "fused":  # 8 ranks, M_local 1024/4096/16384, f16 and bf16, + subgroup (0,2,4)
-        for path in ("2sm", "1sm"):
+        for path in ("auto", "2sm", "1sm"):
             for M in (1024, 4096, 16384):
                 for dt in ("f16", "bf16"):
                     pts.append((None, replace(FUSED, M=M, dtype=dt, path=path)))
