@@ -7,7 +7,8 @@ the largest configurations of the workload (the default, ``--preset largest``):
      (normal(0,1)), explicit tile 8x256, 148 programs, local copy first then
      peers rotated (tensor-map path, runs of tiles claimed per program);
   2. fused matmul + all-gather: W=8, M_local=16384, N=3584, K=8192, f16 in,
-     f32 accumulate, f16 out, 128x256 tcgen05 tiles (256x256 per CTA pair),
+     f32 accumulate, f16 out, 128x512 output tiles per CTA (two 128x256
+     tcgen05 MMA tiles sharing each A stage; 256x512 per CTA pair),
      inputs normal(0,1)/sqrt(K).
 ``--preset small`` runs the smaller step instead: the W=8 4096 x 4096 f16
 all-gather (uniform[-1,1]) and the fused product at M_local=1024.  Every
@@ -81,7 +82,9 @@ class FusedCfg:
     programs: int = 0  # 0: one CTA per SM
     start: int = 0
     stride: int = 1
-    path: str = "auto"  # auto / 1sm / 2sm / 2sm_wide
+    path: str = "auto"  # auto / 1sm / 2sm
+    bm: int = 128       # the output tile of one CTA: 128 x 512 (two MMA tiles sharing A,
+    bn: int = 512       # on CTA pairs) or 128 x 256
 
     def members(self):
         return [self.start + i * self.stride for i in range(self.W)]
@@ -91,7 +94,11 @@ class FusedCfg:
             f" group(start={self.start},stride={self.stride})"
         kern = "" if self.path == "auto" else f" {self.path}"
         return (f"matmul_all_gather W={self.W} M_local={self.M} N={self.N} K={self.K} "
-                f"{self.dtype} tile 128x256{grp}{kern}")
+                f"{self.dtype} tile {self.bm}x{self.bn}{grp}{kern}")
+
+    @property
+    def tile(self):
+        return (self.bm, self.bn)
 
 
 ES = {"f16": 2, "bf16": 2, "f32": 4}
@@ -397,7 +404,7 @@ def config_block(peaks, peak_src, g, f):
                              "values": "uniform[-1,1]" if g.values == "uniform" else "normal(0,1)"}
     if f:
         cfg["matmul_all_gather"] = {"W": f.W, "M_local": f.M, "N": f.N, "K": f.K,
-                                    "dtype": f.dtype, "tile": [128, 256],
+                                    "dtype": f.dtype, "tile": [f.bm, f.bn],
                                     "group": [f.start, f.stride, f.W],
                                     "values": "normal(0,1)/sqrt(K)"}
     cfg["l2"] = (f"inputs larger than L2 ({touched / 1e9:.2f} GB of algorithmic traffic per step)"
@@ -514,19 +521,19 @@ def sweep_points(name: str):
         for p in (8, 16, 32, 64, 148):  # W single-rank launches in turn
             pts.append((replace(GATHER, programs=p, kind="ranks"), None))
     elif name == "cublas":  # the fused kernel and cuBLAS on the plain GEMM of the same size
-        for path in ("auto", "2sm"):
+        for bn, path in ((512, "auto"), (256, "2sm")):
             for M in (1024, 4096, 16384):
                 for dt in ("f16", "bf16"):
-                    pts.append((None, replace(FUSED, M=M, dtype=dt, path=path)))
+                    pts.append((None, replace(FUSED, M=M, dtype=dt, path=path, bn=bn)))
     elif name == "fused":  # 8 ranks, M_local 1024/4096/16384, f16 and bf16, + subgroup (0,2,4)
-        for path in ("auto", "2sm", "1sm"):
+        for bn, path in ((512, "auto"), (256, "2sm"), (256, "1sm")):
             for M in (1024, 4096, 16384):
                 for dt in ("f16", "bf16"):
-                    pts.append((None, replace(FUSED, M=M, dtype=dt, path=path)))
+                    pts.append((None, replace(FUSED, M=M, dtype=dt, path=path, bn=bn)))
             for M in (4096, 16384):
                 for dt in ("f16", "bf16"):
                     pts.append((None, replace(FUSED, M=M, dtype=dt, W=4, start=0, stride=2,
-                                              path=path)))
+                                              path=path, bn=bn)))
     else:
         raise SystemExit(f"unknown sweep {name}")
     return pts
@@ -634,7 +641,7 @@ def run_sweep(args):
             else:
                 gg.matmul_all_gather(sh.heap, -1, sh.ptr(f.start, offs["f_a"]), f.K, Bd, f.N,
                                      sh.ptr(f.start, offs["f_out"]), f.N, f.M, f.N, f.K,
-                                     gg_inputs.DTYPES[f.dtype], gg.FUSED_TILE, f.programs,
+                                     gg_inputs.DTYPES[f.dtype], f.tile, f.programs,
                                      (f.start, f.stride, f.W), status=status, path=f.path)
 
         t_rg, t_rf = roofline_times(peaks, g, f)
@@ -809,7 +816,7 @@ def main():
         if f:
             gg.matmul_all_gather(heap.heap, -1, heap.ptr(f.start, offs["f_a"]), f.K, b_dev, f.N,
                                  heap.ptr(f.start, offs["f_out"]), f.N, f.M, f.N, f.K, fdt,
-                                 gg.FUSED_TILE, f.programs, (f.start, f.stride, f.W),
+                                 f.tile, f.programs, (f.start, f.stride, f.W),
                                  status=status, stream=strm, path=f.path)
 
     def step(ev=None):
@@ -822,7 +829,7 @@ def main():
         if f:
             gg.matmul_all_gather(sh.heap, -1, sh.ptr(f.start, offs["f_a"]), f.K, Bd, f.N,
                                  sh.ptr(f.start, offs["f_out"]), f.N, f.M, f.N, f.K, fdt,
-                                 gg.FUSED_TILE, f.programs, (f.start, f.stride, f.W),
+                                 f.tile, f.programs, (f.start, f.stride, f.W),
                                  status=status, stream=stream, path=f.path)
         if ev is not None:
             ev[2].record(stream)
@@ -1044,9 +1051,10 @@ def main():
         f_tfs = fused_flops(f) / (f_ms * 1e-3) / 1e12
         chosen = gg.matmul_all_gather_plan(sh.heap, -1, sh.ptr(f.start, offs["f_a"]), f.K, Bd, f.N,
                                            sh.ptr(f.start, offs["f_out"]), f.N, f.M, f.N, f.K,
-                                           fdt, gg.FUSED_TILE, f.programs,
+                                           fdt, f.tile, f.programs,
                                            (f.start, f.stride, f.W), f.path)
-        fk = {"1sm": "mag1_kernel", "2sm": "mag2_kernel", "2sm_wide": "mag2w_kernel"}[chosen]
+        fk = "mag1_kernel" if chosen == "1sm" else ("mag2w_kernel" if f.bn == 512 else
+                                                     "mag2_kernel")
         kernels["matmul_all_gather"] = {"kernel": fk, "ms": f_ms, "TFLOP/s": f_tfs,
                                         "roofline_ms": 1e3 * t_rf, "frac": f_tfs / tc_peak,
                                         "bound": "tensor", "algorithmic_flops": fused_flops(f),

@@ -14,10 +14,11 @@ from dataclasses import dataclass
 import torch
 
 from ._lib import (GG_AG_AUTO, GG_AG_BULK, GG_AG_TMA, GG_AG_VECTOR, GG_BF16, GG_MAG_1SM, GG_MAG_2SM,
-                   GG_MAG_2SM_WIDE, GG_MAG_AUTO, GG_COLL_ALL_GATHER, GG_COLL_ALL_GATHER_PARTITIONED,
+                   GG_MAG_AUTO, GG_COLL_ALL_GATHER, GG_COLL_ALL_GATHER_PARTITIONED,
                    GG_COLL_ALL_TO_ALL, GG_ERR_ALIGNMENT,
                    GG_ERR_CUDA, GG_ERR_INVALID_ARG, GG_ERR_NOT_IN_HEAP, GG_ERR_TIMEOUT,
                    GG_ERR_UNSUPPORTED, GG_F16, GG_F32, GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N,
+                   GG_FUSED_BLOCK_N_WIDE,
                    GG_CLAIM_ALWAYS, GG_CLAIM_AUTO, GG_CLAIM_NEVER, GG_MAX_WORLD, GG_OK,
                    GG_WORKSPACE_SLOT_BYTES,
                    GGError, Group, Tile, check, lib, LIB_PATH)
@@ -31,14 +32,14 @@ __all__ = [
     "get_claim_policy", "CLAIM_POLICIES", "set_wait_limit_ns",
     "get_wait_limit_ns", "debug_inject_stall", "device_status", "clear_device_status",
     "SymmetricHeap", "Heap", "GGError", "DTYPE_CODES", "PATHS",
-    "FUSED_TILE", "FUSED_PATHS",
+    "FUSED_TILE", "FUSED_TILE_WIDE", "FUSED_PATHS",
 ]
 
 DTYPE_CODES = {torch.float16: GG_F16, torch.bfloat16: GG_BF16, torch.float32: GG_F32}
 PATHS = {"auto": GG_AG_AUTO, "bulk": GG_AG_BULK, "vector": GG_AG_VECTOR, "tma": GG_AG_TMA}
-FUSED_PATHS = {"auto": GG_MAG_AUTO, "1sm": GG_MAG_1SM, "2sm": GG_MAG_2SM,
-               "2sm_wide": GG_MAG_2SM_WIDE}
-FUSED_TILE = (GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N)
+FUSED_PATHS = {"auto": GG_MAG_AUTO, "1sm": GG_MAG_1SM, "2sm": GG_MAG_2SM}
+FUSED_TILE = (GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N)             # 128 x 256 per CTA
+FUSED_TILE_WIDE = (GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N_WIDE)   # 128 x 512 per CTA (CTA pairs)
 CLAIM_POLICIES = {"auto": GG_CLAIM_AUTO, "always": GG_CLAIM_ALWAYS, "never": GG_CLAIM_NEVER}
 
 
@@ -229,15 +230,14 @@ def matmul_all_gather_plan(heap: Heap, rank: int, A, lda: int, B, ldb: int, outp
                            M: int, N: int, K: int, dtype, tile: tuple[int, int],
                            comm_programs: int, group: tuple[int, int, int],
                            path: str = "auto") -> str:
-    """Validate without launching; returns the kernel a launch would run
-    ("1sm", "2sm", "2sm_wide"; "none" when there is nothing to launch)."""
+    """Validate without launching; returns the kernel variant a launch would
+    run ("1sm" or "2sm"; "none" when there is nothing to launch)."""
     chosen = ctypes.c_int()
     check(lib.gg_matmul_all_gather_plan(heap.handle, rank, _ptr(A), lda, _ptr(B), ldb,
                                         _ptr(output), ld_out, M, N, K, _dtype(dtype), Tile(*tile),
                                         comm_programs, Group(*group), FUSED_PATHS[path],
                                         ctypes.byref(chosen)))
-    return {GG_MAG_AUTO: "none", GG_MAG_1SM: "1sm", GG_MAG_2SM: "2sm",
-            GG_MAG_2SM_WIDE: "2sm_wide"}[chosen.value]
+    return {GG_MAG_AUTO: "none", GG_MAG_1SM: "1sm", GG_MAG_2SM: "2sm"}[chosen.value]
 
 
 def set_claim_policy(policy: str) -> None:

@@ -21,11 +21,11 @@ GG_ERR_TIMEOUT = -6
 
 GG_F16, GG_BF16, GG_F32 = 0, 1, 2
 GG_AG_AUTO, GG_AG_BULK, GG_AG_VECTOR, GG_AG_TMA = 0, 1, 2, 3
-GG_MAG_AUTO, GG_MAG_1SM, GG_MAG_2SM, GG_MAG_2SM_WIDE = 0, 1, 2, 3
+GG_MAG_AUTO, GG_MAG_1SM, GG_MAG_2SM = 0, 1, 2
 GG_COLL_ALL_GATHER, GG_COLL_ALL_GATHER_PARTITIONED, GG_COLL_ALL_TO_ALL = 0, 1, 2
 GG_MAX_WORLD = 64
 GG_MAX_HEAPS = 1024
-GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N = 128, 256
+GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N, GG_FUSED_BLOCK_N_WIDE = 128, 256, 512
 GG_WORKSPACE_SLOT_BYTES = 128
 GG_CLAIM_AUTO, GG_CLAIM_ALWAYS, GG_CLAIM_NEVER = 0, 1, 2
 

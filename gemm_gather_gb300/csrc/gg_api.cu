@@ -606,6 +606,24 @@ gg_status gg_all_gather(const gg_heap *heap, int rank, const void *input, int64_
 
 namespace {
 
+// Path checks of the fused calls (before the argument checks of prepare_fused).
+gg_status check_fused_path(gg_mag_path path, gg_tile tile, int comm_programs)
+{
+    if (path != GG_MAG_AUTO && path != GG_MAG_1SM && path != GG_MAG_2SM)
+        return fail(GG_ERR_INVALID_ARG, "unknown fused path %d", (int)path);
+    if (path == GG_MAG_2SM && comm_programs < 2)
+        return fail(GG_ERR_INVALID_ARG, "the 2-SM path needs comm_programs >= 2 (one CTA pair)");
+    if (tile.block_m == GG_FUSED_BLOCK_M && tile.block_n == GG_FUSED_BLOCK_N_WIDE) {
+        if (path == GG_MAG_1SM)
+            return fail(GG_ERR_UNSUPPORTED, "the %dx%d tile runs on CTA pairs only, not the 1-SM "
+                        "path (tiles are never remapped)", GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N_WIDE);
+        if (comm_programs < 2)
+            return fail(GG_ERR_INVALID_ARG, "the %dx%d tile needs comm_programs >= 2 (one CTA "
+                        "pair)", GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N_WIDE);
+    }
+    return GG_OK;
+}
+
 gg_status prepare_fused(const gg_heap *heap, int rank, const void *A, int64_t lda, const void *B,
                         int64_t ldb, void *output, int64_t ld_out, int64_t M, int64_t N,
                         int64_t K, gg_dtype dtype, gg_tile tile, int comm_programs,
@@ -619,11 +637,13 @@ gg_status prepare_fused(const gg_heap *heap, int rank, const void *A, int64_t ld
         return st;
     if (dtype != GG_F16 && dtype != GG_BF16)
         return fail(GG_ERR_UNSUPPORTED, "matmul_all_gather takes GG_F16 or GG_BF16");
-    if (tile.block_m != GG_FUSED_BLOCK_M || tile.block_n != GG_FUSED_BLOCK_N)
+    if (tile.block_m != GG_FUSED_BLOCK_M ||
+        (tile.block_n != GG_FUSED_BLOCK_N && tile.block_n != GG_FUSED_BLOCK_N_WIDE))
         return fail(GG_ERR_UNSUPPORTED,
-                    "fused tile %dx%d is not supported; this build runs %dx%d (tiles are never "
-                    "remapped)",
-                    tile.block_m, tile.block_n, GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N);
+                    "fused tile %dx%d is not supported; this build runs %dx%d and %dx%d (tiles are "
+                    "never remapped)",
+                    tile.block_m, tile.block_n, GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N,
+                    GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N_WIDE);
     if (M < 0 || N < 0 || K < 0)
         return fail(GG_ERR_INVALID_ARG, "M, N and K must be >= 0");
     if (lda < K || ldb < N || ld_out < N)
@@ -663,6 +683,7 @@ gg_status prepare_fused(const gg_heap *heap, int rank, const void *A, int64_t ld
     f.N = N;
     f.K = K;
     f.is_bf16 = dtype == GG_BF16;
+    f.wide = tile.block_n == GG_FUSED_BLOCK_N_WIDE;
     f.heap_base = heap->base;
     f.part_bytes = heap->part;
     f.num_heaps = heap->H;
@@ -724,16 +745,14 @@ gg_status gg_matmul_all_gather_path(const gg_heap *heap, int rank, const void *A
                                     int comm_programs, gg_group group, int *dev_status,
                                     gg_stream_t stream, gg_mag_path path)
 {
-    if (path != GG_MAG_AUTO && path != GG_MAG_1SM && path != GG_MAG_2SM &&
-        path != GG_MAG_2SM_WIDE)
-        return fail(GG_ERR_INVALID_ARG, "unknown fused path %d", (int)path);
-    if ((path == GG_MAG_2SM || path == GG_MAG_2SM_WIDE) && comm_programs < 2)
-        return fail(GG_ERR_INVALID_ARG, "the 2-SM paths need comm_programs >= 2 (one CTA pair)");
+    gg_status st = check_fused_path(path, tile, comm_programs);
+    if (st != GG_OK)
+        return st;
     gg::FusedArgs f;
     static thread_local gg::OutMaps maps;
     bool launch = false;
-    gg_status st = prepare_fused(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype, tile,
-                                 comm_programs, group, dev_status, &f, &maps, &launch);
+    st = prepare_fused(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype, tile,
+                       comm_programs, group, dev_status, &f, &maps, &launch);
     if (st != GG_OK || !launch)
         return st;
     st = resolve_status(&f.status);
@@ -763,6 +782,9 @@ gg_status gg_matmul_all_gather_check(const gg_heap *heap, int rank, const void *
                                      int64_t M, int64_t N, int64_t K, gg_dtype dtype,
                                      gg_tile tile, int comm_programs, gg_group group)
 {
+    gg_status st = check_fused_path(GG_MAG_AUTO, tile, comm_programs);
+    if (st != GG_OK)
+        return st;
     gg::FusedArgs f;
     bool launch = false;
     return prepare_fused(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype, tile,
@@ -777,17 +799,15 @@ gg_status gg_matmul_all_gather_plan(const gg_heap *heap, int rank, const void *A
 {
     if (chosen)
         *chosen = GG_MAG_AUTO;
-    if (path != GG_MAG_AUTO && path != GG_MAG_1SM && path != GG_MAG_2SM &&
-        path != GG_MAG_2SM_WIDE)
-        return fail(GG_ERR_INVALID_ARG, "unknown fused path %d", (int)path);
-    if ((path == GG_MAG_2SM || path == GG_MAG_2SM_WIDE) && comm_programs < 2)
-        return fail(GG_ERR_INVALID_ARG, "the 2-SM paths need comm_programs >= 2 (one CTA pair)");
+    gg_status st = check_fused_path(path, tile, comm_programs);
+    if (st != GG_OK)
+        return st;
     gg::FusedArgs f;
     bool launch = false;
-    gg_status st = prepare_fused(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype, tile,
-                                 comm_programs, group, nullptr, &f, nullptr, &launch);
+    st = prepare_fused(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype, tile,
+                       comm_programs, group, nullptr, &f, nullptr, &launch);
     if (st == GG_OK && launch && chosen)
-        *chosen = (gg_mag_path)gg::fused_variant(N, comm_programs, (int)path);
+        *chosen = (gg_mag_path)gg::fused_variant(comm_programs, (int)path);
     return st;
 }
 

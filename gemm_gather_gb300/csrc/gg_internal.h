@@ -98,26 +98,19 @@ struct FusedArgs {
     uint64_t wait_limit_ns;
     int inject_stall;  // test hook: CTA 0 never arms its first ring stage
     int b_boxes3d;     // set by the launcher: B stages load as one 3-d box
+    int wide;          // 128 x 512 CTA tiles (256 x 512 per pair): two MMAs per A stage
     int tn_group;      // set by the launcher: tile columns per group of the tile order
 };
 
-// Fused kernel variants: 1 = 1-SM 128 x 256 tiles, 2 = 2-SM 256 x 256 pair
-// tiles, 3 = 2-SM 256 x 512 pair tiles; 0 = automatic.
-// The variant a launch runs for `requested` (0..3): one CTA runs the 1-SM
-// kernel; the automatic choice takes 256 x 512 pair tiles unless they pad N
-// by more than 1/16 beyond what 256-column tiles pad, else 256 x 256.
-inline int fused_variant(int64_t N, int programs, int requested)
+// Fused kernel variants: 1 = 1-SM (one CTA per 128 x 256 tile), 2 = CTA
+// pairs (256 x 256 pair tiles, or 256 x 512 with FusedArgs::wide); 0 =
+// automatic.  The variant a launch runs for `requested`:
+inline int fused_variant(int programs, int requested)
 {
-    if (requested == 1 || programs < 2)
-        return 1;
-    if (requested == 2 || requested == 3)
-        return requested;
-    const int64_t cols_narrow = (N + 255) / 256 * 256;
-    const int64_t cols_wide = (N + 511) / 512 * 512;
-    return 16 * cols_wide <= 17 * cols_narrow ? 3 : 2;
+    return requested == 1 || programs < 2 ? 1 : 2;
 }
 
-// variant: 0 = automatic, 1 / 2 / 3 as fused_variant
+// variant: 0 = automatic, 1 / 2 as fused_variant
 cudaError_t launch_matmul_all_gather(const FusedArgs &a, const OutMaps &out, int programs,
                                      int variant, cudaStream_t s, const char **why);
 

@@ -55,7 +55,7 @@ constexpr int kMaxStages = 8;
 // +0-2.5%).
 constexpr bool kBBoxes3d = true;
 // Bytes of B one column group of the tile order may span (see tile_coord):
-// 256-column tiles / 512-column tiles (measured best at N=3584, K=8192:
+// 256-column / 512-column pair tiles (measured best at N=3584, K=8192:
 // groups of 7 narrow tiles, one group of 7 wide ones).
 constexpr int64_t kBGroupBytes = 32ll << 20;
 constexpr int64_t kBGroupBytesWide = 64ll << 20;
@@ -1146,9 +1146,8 @@ cudaError_t launch_matmul_all_gather(const FusedArgs &a, const OutMaps &out, int
             return cudaErrorInvalidValue;
         }
     }
-    const int chosen = fused_variant(a.N, programs, variant);
-    const bool two_sm = chosen != 1;
-    const bool wide_tiles = chosen == 3;  // 256 x 512 pair tiles
+    const bool two_sm = fused_variant(programs, variant) == 2;
+    const bool wide_tiles = two_sm && a.wide;  // 256 x 512 pair tiles
     const int bk = two_sm ? Geo<2>::kBK : Geo<1>::kBK;  // K rows of one B box
     FusedArgs args = a;
     args.b_boxes3d = 0;

@@ -71,9 +71,12 @@ typedef struct gg_heap gg_heap; /* opaque host handle */
 #define GG_MAX_WORLD 64
 #define GG_MAX_HEAPS 1024
 
-/* Supported fused (matmul_all_gather) tile: the tcgen05 tile of one CTA. */
+/* Supported fused (matmul_all_gather) tiles: the output tile of one CTA,
+ * {GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N} or {GG_FUSED_BLOCK_M,
+ * GG_FUSED_BLOCK_N_WIDE}. */
 #define GG_FUSED_BLOCK_M 128
 #define GG_FUSED_BLOCK_N 256
+#define GG_FUSED_BLOCK_N_WIDE 512
 
 /* ---------------------------------------------------------------------------
  * gg_heap_create — describe a symmetric heap of `num_heaps` partitions of
@@ -323,14 +326,22 @@ gg_status gg_collective_check(gg_collective kind, const gg_heap *heap, int rank,
  * rank >= 0: only that member computes and gathers its block; `A` is any
  *   device pointer.  rank == -1: every member, in one launch; `A` is then a
  *   symmetric heap buffer.
- * tile: must be {GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N}; anything else returns
- *   GG_ERR_UNSUPPORTED (never remapped).
+ * tile: the output tile of one CTA, exactly as given (never remapped):
+ *   {GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N} = 128 x 256: one tcgen05 MMA tile
+ *     per CTA, 256 x 256 per CTA pair (or 128 x 256 on the 1-SM path);
+ *   {GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N_WIDE} = 128 x 512: two 128 x 256 MMA
+ *     tiles side by side per CTA, sharing each A stage, 256 x 512 per CTA
+ *     pair; needs the CTA pairs (comm_programs >= 2, not GG_MAG_1SM).  It
+ *     reads a quarter fewer operand bytes per MMA and is the faster choice
+ *     wherever N is not padded much more by 512-column tiles (N = 3584:
+ *     95-98% of cuBLAS's rate on the plain GEMM, against 89-90%).
+ *   Anything else returns GG_ERR_UNSUPPORTED.
  * Alignment (GG_ERR_ALIGNMENT otherwise): A, B, output 16-byte aligned;
  *   lda, ldb, ld_out multiples of 8; N a multiple of 8.
  * comm_programs: number of persistent CTAs (one per SM at most is useful).
  *   By default they run as CTA pairs (comm_programs/2 clusters of two CTAs,
- *   a 256 x 512 output tile per pair, or 256 x 256 where that pads N
- *   noticeably less); a single program runs alone on 128 x 256 tiles.
+ *   each pair on twice the tile's rows); a single program runs alone on
+ *   128 x 256 tiles.
  * dev_status: as for gg_all_gather (NULL: the library's status word).
  * M, N or K == 0: nothing is launched, GG_OK (with K == 0 nothing is
  *   written either).
@@ -342,20 +353,12 @@ gg_status gg_matmul_all_gather(const gg_heap *heap, int rank, const void *A, int
                                int *dev_status, gg_stream_t stream);
 
 /* Kernel variants of gg_matmul_all_gather (same arguments and result):
- *   GG_MAG_AUTO       2-SM pairs when comm_programs >= 2 (256 x 512 tiles
- *                     unless they pad N noticeably more, see
- *                     gg_matmul_all_gather_plan), else 1-SM
- *   GG_MAG_1SM        one CTA per 128 x 256 tile (tcgen05.mma.cta_group::1)
- *   GG_MAG_2SM        a CTA pair per 256 x 256 tile (tcgen05.mma.cta_group::2);
- *                     needs comm_programs >= 2 (else GG_ERR_INVALID_ARG)
- *   GG_MAG_2SM_WIDE   a CTA pair per 256 x 512 tile: two MMAs share each A
- *                     stage; needs comm_programs >= 2 */
-typedef enum {
-    GG_MAG_AUTO = 0,
-    GG_MAG_1SM = 1,
-    GG_MAG_2SM = 2,
-    GG_MAG_2SM_WIDE = 3
-} gg_mag_path;
+ *   GG_MAG_AUTO  2-SM pairs when comm_programs >= 2, else 1-SM
+ *   GG_MAG_1SM   one CTA per 128 x 256 tile (tcgen05.mma.cta_group::1);
+ *                GG_ERR_UNSUPPORTED for the 128 x 512 tile
+ *   GG_MAG_2SM   a CTA pair per two tiles (tcgen05.mma.cta_group::2);
+ *                needs comm_programs >= 2 (else GG_ERR_INVALID_ARG) */
+typedef enum { GG_MAG_AUTO = 0, GG_MAG_1SM = 1, GG_MAG_2SM = 2 } gg_mag_path;
 
 gg_status gg_matmul_all_gather_path(const gg_heap *heap, int rank, const void *A, int64_t lda,
                                     const void *B, int64_t ldb, void *output, int64_t ld_out,
@@ -364,12 +367,9 @@ gg_status gg_matmul_all_gather_path(const gg_heap *heap, int rank, const void *A
                                     gg_stream_t stream, gg_mag_path path);
 
 /* Validate a gg_matmul_all_gather_path call exactly as the launching call
- * does and launch nothing; *chosen (nullable) receives the kernel a launch
- * would run: GG_MAG_1SM (a single program, or asked for), GG_MAG_2SM or
- * GG_MAG_2SM_WIDE.  For GG_MAG_AUTO with comm_programs >= 2 that is the wide
- * 256 x 512 pair tile unless it pads N by more than 1/16 beyond what
- * 256-column tiles pad (N = 256: GG_MAG_2SM; N = 3584: GG_MAG_2SM_WIDE).
- * GG_MAG_AUTO when there is nothing to launch. */
+ * does and launch nothing; *chosen (nullable) receives the kernel variant a
+ * launch would run: GG_MAG_1SM (a single program, or asked for) or
+ * GG_MAG_2SM; GG_MAG_AUTO when there is nothing to launch. */
 gg_status gg_matmul_all_gather_plan(const gg_heap *heap, int rank, const void *A, int64_t lda,
                                     const void *B, int64_t ldb, void *output, int64_t ld_out,
                                     int64_t M, int64_t N, int64_t K, gg_dtype dtype,

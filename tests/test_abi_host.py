@@ -183,30 +183,29 @@ def plan(heap, path="auto", **kw):
                                      a["tile"], a["comm_programs"], a["group"], path)
 
 
-@pytest.mark.parametrize("N,want", [
-    (512, "2sm_wide"), (3584, "2sm_wide"), (264, "2sm_wide"),   # same padding either way
-    (256, "2sm"), (8, "2sm"), (768, "2sm"), (1280, "2sm"),       # 256-column tiles pad less
-    (4352, "2sm_wide"),                                           # 17 x 256: 1/16 more padding
-    (2304, "2sm"),                                                # 9 x 256: 1/9 more padding
-])
-def test_fused_plan_automatic_choice(heap, N, want):
-    """The automatic fused path takes 256 x 512 pair tiles unless they pad N
-    by more than 1/16 beyond what 256-column tiles pad."""
-    assert plan(heap, N=N) == want
-
-
-def test_fused_plan_explicit_paths(heap):
+def test_fused_plan_variants(heap):
+    """The tile is the CTA's output tile, never remapped; the path only picks
+    one CTA or CTA pairs."""
+    assert plan(heap) == "2sm"
     assert plan(heap, comm_programs=1) == "1sm"
     assert plan(heap, path="1sm") == "1sm"
     assert plan(heap, path="2sm") == "2sm"
-    assert plan(heap, path="2sm_wide", N=256) == "2sm_wide"
+    assert plan(heap, tile=gg.FUSED_TILE_WIDE) == "2sm"
+    assert plan(heap, tile=gg.FUSED_TILE_WIDE, path="2sm", N=256) == "2sm"
     assert plan(heap, M=0) == "none"
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(tile=gg.FUSED_TILE_WIDE, path="1sm"), _lib.GG_ERR_UNSUPPORTED),   # pairs only
+    (dict(tile=gg.FUSED_TILE_WIDE, comm_programs=1), _lib.GG_ERR_INVALID_ARG),
+    (dict(path="2sm", comm_programs=1), _lib.GG_ERR_INVALID_ARG),
+    (dict(tile=(256, 128)), _lib.GG_ERR_UNSUPPORTED),
+    (dict(tile=(128, 384)), _lib.GG_ERR_UNSUPPORTED),
+])
+def test_fused_plan_rejects(heap, kw, status):
     with pytest.raises(gg.GGError) as e:
-        plan(heap, path="2sm_wide", comm_programs=1)
-    assert e.value.status == _lib.GG_ERR_INVALID_ARG
-    with pytest.raises(gg.GGError) as e:
-        plan(heap, tile=(256, 128))
-    assert e.value.status == _lib.GG_ERR_UNSUPPORTED
+        plan(heap, **kw)
+    assert e.value.status == status, str(e.value)
 
 
 def test_fused_valid_calls(heap):
@@ -215,6 +214,10 @@ def test_fused_valid_calls(heap):
     mag(heap, dtype=torch.bfloat16)
     mag(heap, K=0)
     mag(heap, M=0)
+    mag(heap, tile=gg.FUSED_TILE_WIDE)
+    with pytest.raises(gg.GGError) as e:           # the wide tile needs CTA pairs
+        mag(heap, tile=gg.FUSED_TILE_WIDE, comm_programs=1)
+    assert e.value.status == _lib.GG_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("kw,status", [

@@ -63,9 +63,11 @@ def test_gather_wait_limit_reports_timeout(oracle, short_waits, path):
     assert np.array_equal(got, host), first_diff(got, host, lay)
 
 
-@pytest.mark.parametrize("path", ["1sm", "2sm", "2sm_wide"])
+@pytest.mark.parametrize("path", ["1sm", "2sm", "wide"])
 def test_fused_wait_limit_reports_timeout(oracle, short_waits, path):
     import gemm_gather_gb300 as gg
+    from tests.test_gpu_fused import kernel_args
+    path, tile = kernel_args(path)
     W, M, N, K = 2, 512, 1024, 2048
     lay = hi.make_layout(W, W, M, N, 2, ld_in=K)
     host = hi.sentinel_heap(lay)
@@ -79,7 +81,7 @@ def test_fused_wait_limit_reports_timeout(oracle, short_waits, path):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     gg.clear_device_status()
     gg.matmul_all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), K, Bd, N, sh.ptr(0, lay.out_off), N,
-                         M, N, K, torch.float16, gg.FUSED_TILE, 8, (0, 1, W), status=status,
+                         M, N, K, torch.float16, tile, 8, (0, 1, W), status=status,
                          path=path)
     torch.cuda.synchronize()
     assert int(status.item()) == TIMEOUT
@@ -88,7 +90,7 @@ def test_fused_wait_limit_reports_timeout(oracle, short_waits, path):
     gg.set_wait_limit_ns(0)
     status.zero_()
     gg.matmul_all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), K, Bd, N, sh.ptr(0, lay.out_off), N,
-                         M, N, K, torch.float16, gg.FUSED_TILE, 8, (0, 1, W), status=status,
+                         M, N, K, torch.float16, tile, 8, (0, 1, W), status=status,
                          path=path)
     got = download(sh)
     assert int(status.item()) == 0
@@ -98,14 +100,16 @@ def test_fused_wait_limit_reports_timeout(oracle, short_waits, path):
     assert np.array_equal(got, host), first_diff(got, host, lay)
 
 
-@pytest.mark.parametrize("kind", ["bulk", "tma", "1sm", "2sm", "2sm_wide"])
+@pytest.mark.parametrize("kind", ["bulk", "tma", "1sm", "2sm", "wide"])
 def test_timeout_without_status_word_is_reported(oracle, short_waits, kind):
     """A launch given no status word (NULL) reports a wait that gave up in the
     library's status word of the device: no early stop goes unreported.  After
     clearing it, the same launch runs normally, leaves the word at 0 and gives
     the oracle's heap."""
     import gemm_gather_gb300 as gg
-    fused = kind in ("1sm", "2sm", "2sm_wide")
+    from tests.test_gpu_fused import kernel_args
+    fused = kind in ("1sm", "2sm", "wide")
+    path, tile = kernel_args(kind) if fused else (kind, None)
     if fused:
         W, M, N, K = 2, 512, 1024, 2048
         lay = hi.make_layout(W, W, M, N, 2, ld_in=K)
@@ -124,11 +128,11 @@ def test_timeout_without_status_word_is_reported(oracle, short_waits, kind):
         if fused:
             gg.matmul_all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), K, Bd, N,
                                  sh.ptr(0, lay.out_off), N, M, N, K, torch.float16,
-                                 gg.FUSED_TILE, 8, (0, 1, W), status=None, path=kind)
+                                 tile, 8, (0, 1, W), status=None, path=path)
         else:
             gg.all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), lay.ld_in, sh.ptr(0, lay.out_off),
                           lay.ld_out, lay.M, lay.N, torch.float16, (8, 256), 4, (0, 1, 4),
-                          status=None, path=kind)
+                          status=None, path=path)
 
     gg.clear_device_status()
     assert gg.device_status() == 0

@@ -129,17 +129,19 @@ FUSED_ALL_ROWS_UP_TO = 1024
 FUSED_SAMPLE_ROWS = 256
 
 FUSED_CASES = [
-    # (W, group, M, dtype, path)
-    (8, (0, 1, 8), 1024, torch.float16, "auto"),
+    # (W, group, M, dtype, kernel: "wide" = the bench's 128 x 512 CTA tiles on CTA
+    #  pairs, "2sm" / "1sm" = 128 x 256 CTA tiles on CTA pairs / one CTA)
+    (8, (0, 1, 8), 1024, torch.float16, "wide"),
+    (8, (0, 1, 8), 1024, torch.float16, "2sm"),
     (8, (0, 1, 8), 1024, torch.float16, "1sm"),
-    (8, (0, 1, 8), 4096, torch.float16, "auto"),
-    (8, (0, 1, 8), 4096, torch.float16, "2sm"),       # the 256 x 256 pair kernel
-    (8, (0, 1, 8), 4096, torch.bfloat16, "auto"),
-    (8, (0, 1, 8), 16384, torch.float16, "auto"),
-    (8, (0, 1, 8), 16384, torch.bfloat16, "auto"),
-    (4, (0, 2, 4), 4096, torch.float16, "auto"),
-    (4, (0, 2, 4), 16384, torch.float16, "auto"),
-    (4, (0, 2, 4), 16384, torch.bfloat16, "auto"),
+    (8, (0, 1, 8), 4096, torch.float16, "wide"),
+    (8, (0, 1, 8), 4096, torch.float16, "2sm"),
+    (8, (0, 1, 8), 4096, torch.bfloat16, "wide"),
+    (8, (0, 1, 8), 16384, torch.float16, "wide"),
+    (8, (0, 1, 8), 16384, torch.bfloat16, "wide"),
+    (4, (0, 2, 4), 4096, torch.float16, "wide"),
+    (4, (0, 2, 4), 16384, torch.float16, "wide"),
+    (4, (0, 2, 4), 16384, torch.bfloat16, "wide"),
 ]
 
 
@@ -147,7 +149,9 @@ FUSED_CASES = [
                          ids=lambda c: f"W{c[0]}g{c[1]}_M{c[2]}_{str(c[3])[6:]}_{c[4]}")
 def test_fused_full_size(oracle, case):
     import gemm_gather_gb300 as gg
-    W, group, M, dtype, path = case
+    from tests.test_gpu_fused import kernel_args
+    W, group, M, dtype, kernel = case
+    path, tile = kernel_args(kernel)
     N, K = 3584, 8192
     start, stride, _ = group
     members = [start + i * stride for i in range(W)]
@@ -166,7 +170,7 @@ def test_fused_full_size(oracle, case):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     gg.matmul_all_gather(sh.heap, -1, sh.ptr(start, a_off), K, B, N, sh.ptr(start, out_off), N,
-                         M, N, K, dtype, gg.FUSED_TILE, sms, group, status=status, path=path)
+                         M, N, K, dtype, tile, sms, group, status=status, path=path)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     # every byte: the W copies of every block are identical

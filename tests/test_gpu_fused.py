@@ -44,9 +44,19 @@ def check_tolerance(gpu_vals: np.ndarray, ref: np.ndarray, dtype) -> None:
                            f"{float((err / bound).max()):.3f} x bound")
 
 
+def kernel_args(kernel):
+    """(path, tile) of a kernel id: "1sm" / "2sm" run the 128 x 256 CTA tile on
+    one CTA / CTA pairs; "wide" runs the 128 x 512 CTA tile (CTA pairs)."""
+    import gemm_gather_gb300 as gg
+    if kernel == "wide":
+        return "auto", gg.FUSED_TILE_WIDE
+    return kernel, gg.FUSED_TILE
+
+
 def run_fused(oracle, H, group, M, N, K, dtype, programs, values="int", lda_pad=0,
               ld_out_pad=0, mode="group", seed=0, path="auto"):
     import gemm_gather_gb300 as gg
+    path, tile = kernel_args(path)
     start, stride, W = group
     members = [start + i * stride for i in range(W)]
     lda = (K + 7) // 8 * 8 + lda_pad  # TMA needs 16-byte row pitches
@@ -72,12 +82,12 @@ def run_fused(oracle, H, group, M, N, K, dtype, programs, values="int", lda_pad=
     if mode == "group":
         gg.matmul_all_gather(sh.heap, -1, sh.ptr(members[0], lay.in_off), lda, Bd, N,
                              sh.ptr(members[0], lay.out_off), lay.ld_out, M, N, K, dtype,
-                             gg.FUSED_TILE, programs, group, status=status, path=path)
+                             tile, programs, group, status=status, path=path)
     else:
         for h in members:
             gg.matmul_all_gather(sh.heap, h, sh.ptr(h, lay.in_off), lda, Bd, N,
                                  sh.ptr(h, lay.out_off), lay.ld_out, M, N, K, dtype,
-                                 gg.FUSED_TILE, programs, group, status=status, path=path)
+                                 tile, programs, group, status=status, path=path)
     got = download(sh)
     assert int(status.item()) == 0, int(status.item())
     prods = oracle.matmul_all_gather(host, lay.part_bytes, lay.in_off, lda, _bits(B),
@@ -115,7 +125,7 @@ INT_CASES = [
 ]
 
 
-PATHS = ["1sm", "2sm", "2sm_wide"]
+PATHS = ["1sm", "2sm", "wide"]
 
 
 @pytest.mark.parametrize("path", PATHS)
