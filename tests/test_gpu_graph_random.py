@@ -22,9 +22,11 @@ from tests.gpu_util import device_heap, download, first_diff
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("policy,M,N,programs", [("auto", 48, 512, 16), ("always", 256, 1024, 2)])
-def test_step_captured_in_a_cuda_graph(oracle, policy, M, N, programs):
+@pytest.mark.parametrize("policy,M,N,programs,wide", [("auto", 48, 512, 16, True),
+                                                      ("always", 256, 1024, 2, False)])
+def test_step_captured_in_a_cuda_graph(oracle, policy, M, N, programs, wide):
     import gemm_gather_gb300 as gg
+    fused_tile = gg.FUSED_TILE_WIDE if wide else gg.FUSED_TILE
     W = 4
     Mf, Nf, Kf = 256, 512, 192
     es = 2
@@ -53,7 +55,7 @@ def test_step_captured_in_a_cuda_graph(oracle, policy, M, N, programs):
         gg.all_gather(sh.heap, -1, sh.ptr(0, in_off), N, sh.ptr(0, out_off), N, M, N,
                       torch.float16, (8, 256), programs, (0, 1, W), status=status, stream=stream)
         gg.matmul_all_gather(sh.heap, -1, sh.ptr(0, a_off), Kf, Bd, Nf, sh.ptr(0, c_off), Nf,
-                             Mf, Nf, Kf, torch.float16, gg.FUSED_TILE, 8, (0, 1, W),
+                             Mf, Nf, Kf, torch.float16, fused_tile, 8, (0, 1, W),
                              status=status, stream=stream)
 
     gg.set_claim_policy(policy)
