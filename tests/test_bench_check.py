@@ -99,3 +99,19 @@ def test_check_point_fused_value_outside_tolerance():
         out[f.M + f.M // 2, 7] += 0.25
     with pytest.raises(RuntimeError, match="outside the tolerance"):
         bench.check_point(None, f, sh, offs, B)
+
+
+@pytest.mark.parametrize("preset", ["largest", "small"])
+def test_traffic_entries_cover_the_bench_workloads(preset):
+    """bench.py reports each kernel's measured DRAM traffic by looking its
+    workload string up in profiles/traffic.json; both presets' workloads must
+    have entries (the source hash is checked at run time, not here)."""
+    import json
+    import os
+    g, f = bench.PRESETS[preset]
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as fh:
+        t = json.load(fh)
+    gather = {e["bench_workload"] for e in t["ag_tma_kernel"]}
+    fused = {e["bench_workload"] for e in t["mag2w_kernel" if f.bn == 512 else "mag2_kernel"]}
+    assert g.describe() in gather, g.describe()
+    assert f.describe() in fused, f.describe()
