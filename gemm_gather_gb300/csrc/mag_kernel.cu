@@ -3,10 +3,14 @@
 // heap-base translation hoisted above the K loop).
 //
 // C_r = A_r @ B for every source r of the launch.  Persistent CTAs, one per
-// SM; the default kernel (mag2) runs them as CTA pairs (clusters of 2) that
-// compute 256 x 256 tiles with tcgen05.mma.cta_group::2, the 1-SM kernel
-// (mag1) 128 x 256 tiles.  Tiles are taken in column groups, so that a wave
-// of tiles reads few distinct slices of A and B (see tile_coord).  Per CTA:
+// SM.  Three kernels, chosen by the caller's tile and path:
+//   * mag2w (128 x 512 CTA tile): CTA pairs (clusters of 2) on 256 x 512
+//     tiles, two tcgen05.mma.cta_group::2 per K step sharing the A stage; see
+//     the "wide pair tiles" section below for how it differs from mag2;
+//   * mag2 (128 x 256 CTA tile): CTA pairs on 256 x 256 tiles;
+//   * mag1 (128 x 256 CTA tile, one CTA): 128 x 256 tiles.
+// Tiles are taken in column groups, so that a wave of tiles reads few
+// distinct slices of A and B (see tile_coord).  Per CTA of mag1 / mag2:
 //   * warp 0 (producer): TMA tensor loads of A (128 x 64, K-major) and of the
 //     CTA's columns of B (64-deep, N-major, 64-column boxes; one 3-d box per
 //     stage when N is a multiple of 64) into a ring of 128B-swizzled stages
