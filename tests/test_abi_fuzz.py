@@ -120,7 +120,7 @@ def test_fused_check_accepts_only_in_bounds_requests(seed):
         lda = K + _pick(rng, [0, 8], [3, -8])
         ldb = N + _pick(rng, [0, 8], [2])
         ld_out = N + _pick(rng, [0, 8], [1, -8])
-        tile = _pick(rng, [(128, 256)], [(128, 128), (256, 256)])
+        tile = _pick(rng, [(128, 256), (128, 512)], [(128, 128), (256, 256), (256, 512)])
         programs = _pick(rng, [1, 2, 152], [0, 70000])
         a_off, out_off = _offset(rng), _offset(rng)
         a_home = start if rank == -1 else (rank if 0 <= rank < H else 0)
@@ -136,7 +136,8 @@ def test_fused_check_accepts_only_in_bounds_requests(seed):
         accepted += 1
         if M == 0 or N == 0 or K == 0:
             continue
-        assert dtype in (_lib.GG_F16, _lib.GG_BF16) and tile == (128, 256)
+        assert dtype in (_lib.GG_F16, _lib.GG_BF16) and tile in ((128, 256), (128, 512))
+        assert tile == (128, 256) or programs >= 2  # the wide tile runs on CTA pairs
         a_ext, out_ext = _extent(M, lda, K, 2), _extent(W * M, ld_out, N, 2)
         b_ext = _extent(K, ldb, N, 2)
         out_off = _symmetric_offset(out)
