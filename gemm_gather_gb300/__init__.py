@@ -31,7 +31,7 @@ __all__ = [
     "set_claim_policy",
     "get_claim_policy", "CLAIM_POLICIES", "set_wait_limit_ns",
     "get_wait_limit_ns", "debug_inject_stall", "device_status", "clear_device_status",
-    "SymmetricHeap", "Heap", "GGError", "DTYPE_CODES", "PATHS",
+    "checked_build", "SymmetricHeap", "Heap", "GGError", "DTYPE_CODES", "PATHS",
     "FUSED_TILE", "FUSED_TILE_WIDE", "FUSED_PATHS",
 ]
 
@@ -274,6 +274,12 @@ def device_status(stream=None) -> int:
 def clear_device_status(stream=None) -> None:
     """Reset the library's status word of the current device to 0 (on ``stream``)."""
     check(lib.gg_clear_device_status(_stream(stream)))
+
+
+def checked_build() -> bool:
+    """True when the loaded library is the checked build (GEMM_GATHER_CHECKED=1 at
+    import): the gather kernels bound every access and report GG_ERR_NOT_IN_HEAP."""
+    return bool(lib.gg_checked_build())
 
 
 # --------------------------------------------------------------------------- #

@@ -1,7 +1,11 @@
-"""ctypes loader of libgemm_gather.so (built in-tree by gemm_gather_gb300.build).
+"""ctypes loader of the C-ABI library (built in-tree by gemm_gather_gb300.build).
 
-Importing this module fails loudly when the library has not been built: there
-is no fallback path of any kind.
+The release build, libgemm_gather.so, is loaded unless the environment sets
+GEMM_GATHER_CHECKED=1, which loads the checked build,
+libgemm_gather_checked.so (the same calls with device-side bounds checks in
+the gather kernels; see gg_checked_build in include/gemm_gather.h).  Importing
+this module fails loudly when the chosen library has not been built: there is
+no fallback path of any kind.
 """
 from __future__ import annotations
 
@@ -9,7 +13,9 @@ import ctypes
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "_build", "libgemm_gather.so")
+CHECKED = os.environ.get("GEMM_GATHER_CHECKED", "0") == "1"
+LIB_PATH = os.path.join(HERE, "_build",
+                        "libgemm_gather_checked.so" if CHECKED else "libgemm_gather.so")
 
 GG_OK = 0
 GG_ERR_INVALID_ARG = -1
@@ -41,7 +47,7 @@ EXPORTS = (
     "gg_set_claim_policy", "gg_get_claim_policy",
     "gg_set_wait_limit_ns", "gg_get_wait_limit_ns", "gg_debug_inject_stall",
     "gg_device_status", "gg_clear_device_status",
-    "gg_last_error", "gg_status_string", "gg_version",
+    "gg_last_error", "gg_status_string", "gg_version", "gg_checked_build",
 )
 
 
@@ -99,6 +105,7 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "gg_last_error": ([], ctypes.c_char_p),
         "gg_status_string": ([i32], ctypes.c_char_p),
         "gg_version": ([], i32),
+        "gg_checked_build": ([], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)

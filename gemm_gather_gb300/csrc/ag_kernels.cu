@@ -82,6 +82,37 @@ struct AgShared {
 
 constexpr int kAgHeader = (int)((sizeof(AgShared) + 127) / 128 * 128);
 
+// Checked build (compiled with GG_CHECKED=1 into libgemm_gather_checked.so):
+// device-side checks of the heap-bases table, of every decoded work item and
+// of every raw address the bulk and vector paths form.  A failed check skips
+// the access and stores GG_ERR_NOT_IN_HEAP in the status word.  The release
+// build compiles every check out (kChecked is a constant).
+#ifndef GG_CHECKED
+#define GG_CHECKED 0
+#endif
+constexpr bool kChecked = GG_CHECKED != 0;
+
+// [p, p + n) lies inside [lo, lo + ext).
+__device__ __forceinline__ bool inside(uint64_t lo, int64_t ext, uint64_t p, uint64_t n)
+{
+    return p >= lo && p - lo <= (uint64_t)ext && n <= (uint64_t)ext - (p - lo);
+}
+
+__device__ __noinline__ void bounds_fault(int *status)
+{
+    report_status(status, kStatusNotInHeap);
+}
+
+// The validated output (and heap input) extents at their offsets fit inside
+// one partition.  Uniform over the launch: a kernel that finds otherwise
+// returns before its first access.
+__device__ __forceinline__ bool extents_ok(const GatherArgs &a)
+{
+    return a.out_ext_b > 0 && (uint64_t)a.out_off + (uint64_t)a.out_ext_b <= a.part_bytes &&
+           a.in_ext_b > 0 &&
+           (a.in_abs != nullptr || (uint64_t)a.in_off + (uint64_t)a.in_ext_b <= a.part_bytes);
+}
+
 // The items a vector-path program walks (the whole program is one pipeline):
 // first, first + step, ... and, for the partitioned all-gather, the one
 // destination it serves.  The ring kernels walk a Feed instead.
@@ -225,6 +256,15 @@ __device__ __forceinline__ Item decode_item(const GatherArgs &a, int64_t t)
     it.rows = (int)gg_min64(a.bm, a.M - r0);
     const int64_t c0 = it.tn * a.bn_b;
     it.rb = (uint32_t)gg_min64(a.bn_b, a.row_b - c0);
+    if (kChecked && !(t >= 0 && t < a.total_items && it.g >= 0 && it.g < a.W && it.d >= -1 &&
+                      it.d < a.W && it.tm >= 0 && r0 < a.M && it.tn >= 0 && c0 < a.row_b)) {
+        bounds_fault(a.status);  // an item outside the tile grid: nothing of it is moved
+        it.g = 0;
+        it.d = it.d < 0 ? -1 : 0;
+        it.tm = it.tn = 0;
+        it.rows = 0;
+        it.rb = 0;
+    }
     return it;
 }
 
@@ -268,7 +308,13 @@ __device__ __forceinline__ void load_member_bases(const GatherArgs &a, uint64_t 
                                                   uint64_t *src)
 {
     for (int i = threadIdx.x; i < a.W; i += blockDim.x) {
-        const uint64_t base = a.bases[a.rank_start + i * a.rank_stride];
+        const int h = a.rank_start + i * a.rank_stride;
+        uint64_t base = a.bases[h];
+        if (kChecked && base != a.heap_lo + (uint64_t)h * a.part_bytes) {
+            // the entry disagrees with the heap layout: reported, and not used
+            bounds_fault(a.status);
+            base = a.heap_lo + (uint64_t)h * a.part_bytes;
+        }
         dst[i] = base + (uint64_t)a.out_off;
         src[i] = a.in_abs ? reinterpret_cast<uint64_t>(a.in_abs) : base + (uint64_t)a.in_off;
     }
@@ -285,6 +331,11 @@ __global__ void __launch_bounds__(kAgWarps * 32)
     AgShared &sh = *reinterpret_cast<AgShared *>(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    if (kChecked && !extents_ok(a)) {
+        if (threadIdx.x == 0)
+            bounds_fault(a.status);
+        return;
+    }
 
     load_member_bases(a, sh.dst, sh.src);
     if (threadIdx.x == 0) {
@@ -316,16 +367,35 @@ __global__ void __launch_bounds__(kAgWarps * 32)
             ptx::bulk_wait_read<D>();
             __syncwarp();
         }
-        const Item it = decode_item(a, t);
+        Item it = decode_item(a, t);
         const int st = (int)(issued % stages);
         const uint32_t bar = full0 + 8u * st;
         const uint32_t buf = ring + (uint32_t)st * stage_bytes;
+        bool load_ok = true;
+        if (kChecked) {
+            // the item's rows of its source block, as the loads below address them
+            const uint64_t first = sh.src[it.g] + (uint64_t)(it.tm * a.bm * a.ld_in_b + it.tn * a.bn_b);
+            const uint64_t span = it.rows > 0 ? (uint64_t)(it.rows - 1) * a.ld_in_b + it.rb : 0;
+            load_ok = it.rows > 0 && inside(sh.src[it.g], a.in_ext_b, first, span);
+            // (rows == 0: an item outside the grid, already reported at decode)
+            if (!load_ok) {
+                if (lane == 0 && it.rows > 0)
+                    bounds_fault(a.status);
+                it.rows = 0;  // nothing loaded, nothing stored
+            }
+        }
         if (lane == 0)
             sh.item[warp][st] = it;
         const bool stall = a.inject_stall && issued == 0 && blockIdx.x == 0 && warp == 0;
         ++issued;
         if (stall)
             return;  // test hook: this stage's barrier phase never completes
+        if (kChecked && !load_ok) {
+            if (lane == 0)
+                ptx::mbar_arrive(bar);  // completes the stage's phase with no bytes
+            __syncwarp();
+            return;
+        }
         if (lane == 0)
             ptx::mbar_arrive_expect_tx(bar, (uint32_t)it.rows * it.rb);
         __syncwarp();
@@ -365,6 +435,11 @@ __global__ void __launch_bounds__(kAgWarps * 32)
                     i -= a.W;
                 uint8_t *dst =
                     reinterpret_cast<uint8_t *>(sh.dst[i]) + (row0 + r) * a.ld_out_b + col0;
+                if (kChecked && !inside(sh.dst[i], a.out_ext_b, reinterpret_cast<uint64_t>(dst),
+                                        it.rb)) {
+                    bounds_fault(a.status);
+                    continue;
+                }
                 ptx::bulk_s2g(dst, buf + (uint32_t)r * pitch, it.rb);
             }
             ptx::bulk_commit();
@@ -400,6 +475,11 @@ __global__ void __launch_bounds__(kAgWarps * 32)
     AgShared &sh = *reinterpret_cast<AgShared *>(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    if (kChecked && !extents_ok(a)) {
+        if (threadIdx.x == 0)
+            bounds_fault(a.status);
+        return;
+    }
 
     if (threadIdx.x == 0) {
         for (int w = 0; w < npipe; ++w)
@@ -410,6 +490,8 @@ __global__ void __launch_bounds__(kAgWarps * 32)
     }
     if (threadIdx.x < (unsigned)a.W)
         tma_prefetch(&out.map[threadIdx.x]);
+    if (kChecked)  // the maps come from the host's bases; the device table must agree
+        load_member_bases(a, sh.dst, sh.src);
     __syncthreads();
 
     int dest;
@@ -436,7 +518,9 @@ __global__ void __launch_bounds__(kAgWarps * 32)
         if (lane == 0) {
             const Item it = decode_item(a, t);
             sh.item[warp][st] = it;
-            if (!stall) {  // test hook: a stalled stage's barrier phase never completes
+            if (kChecked && !stall && it.rows == 0) {
+                ptx::mbar_arrive(full0 + 8u * st);  // an item outside the grid: no load
+            } else if (!stall) {  // test hook: a stalled stage's barrier phase never completes
                 const uint32_t bar = full0 + 8u * st;
                 ptx::mbar_arrive_expect_tx(bar, box_bytes);
                 const int h = a.in_abs ? 0 : a.rank_start + it.g * a.rank_stride;
@@ -467,7 +551,9 @@ __global__ void __launch_bounds__(kAgWarps * 32)
         const Item it = sh.item[warp][st];
         const uint32_t buf = ring + (uint32_t)st * stage_bytes;
         const int c0 = (int)it.tn * bn, c1 = (int)(it.tm * a.bm);
-        if (a.mode == kModeGather) {
+        if (kChecked && it.rows == 0) {
+            // an item outside the grid (reported at decode): no store
+        } else if (a.mode == kModeGather) {
             // lane j stores to destination j of the group: the local copy first,
             // peers rotated; `grp` destinations per wait
             for (int j0 = 0; j0 < a.W; j0 += grp) {
@@ -525,6 +611,11 @@ __global__ void __launch_bounds__(kVecThreads) ag_vec_kernel(const GatherArgs a)
     using V = typename VecType<VB>::T;
     __shared__ uint64_t dst[kMaxWorld];
     __shared__ uint64_t src[kMaxWorld];
+    if (kChecked && !extents_ok(a)) {
+        if (threadIdx.x == 0)
+            bounds_fault(a.status);
+        return;
+    }
     load_member_bases(a, dst, src);
     __syncthreads();
 
@@ -553,6 +644,12 @@ __global__ void __launch_bounds__(kVecThreads) ag_vec_kernel(const GatherArgs a)
                                              it[u].tm * a.bm + r;
                         const uint8_t *s = reinterpret_cast<const uint8_t *>(src[it[u].g]) +
                                            srow * a.ld_in_b + it[u].tn * a.bn_b + (int64_t)cc * VB;
+                        if (kChecked && !inside(src[it[u].g], a.in_ext_b,
+                                                reinterpret_cast<uint64_t>(s), VB)) {
+                            bounds_fault(a.status);
+                            valid[u] = false;
+                            continue;
+                        }
                         v[u] = *reinterpret_cast<const V *>(s);
                     }
                 }
@@ -568,10 +665,18 @@ __global__ void __launch_bounds__(kVecThreads) ag_vec_kernel(const GatherArgs a)
                         int i = it[u].g + j;
                         if (i >= a.W)
                             i -= a.W;
+                        if (kChecked && !inside(dst[i], a.out_ext_b, dst[i] + (uint64_t)off, VB)) {
+                            bounds_fault(a.status);
+                            continue;
+                        }
                         *reinterpret_cast<V *>(reinterpret_cast<uint8_t *>(dst[i]) + off) = v[u];
                     }
                 } else {
                     const int i = a.mode == kModePartitioned ? walk.dest : it[u].d;
+                    if (kChecked && !inside(dst[i], a.out_ext_b, dst[i] + (uint64_t)off, VB)) {
+                        bounds_fault(a.status);
+                        continue;
+                    }
                     *reinterpret_cast<V *>(reinterpret_cast<uint8_t *>(dst[i]) + off) = v[u];
                 }
             }

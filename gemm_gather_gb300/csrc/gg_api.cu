@@ -367,6 +367,10 @@ gg_status prepare_gather(const gg_heap *heap, int mode, int rank, const void *in
 
     gg::GatherArgs a{};
     a.bases = heap->dev_table;
+    a.heap_lo = heap->base;
+    a.part_bytes = (uint64_t)heap->part;
+    a.in_ext_b = in_ext;
+    a.out_ext_b = out_ext;
     a.W = W;
     a.rank_start = group.rank_start;
     a.rank_stride = group.rank_stride;
@@ -881,6 +885,11 @@ const char *gg_status_string(gg_status s)
 }
 
 int gg_version(void) { return 100; }
+
+#ifndef GG_CHECKED
+#define GG_CHECKED 0
+#endif
+int gg_checked_build(void) { return GG_CHECKED ? 1 : 0; }
 
 }  // extern "C"
 

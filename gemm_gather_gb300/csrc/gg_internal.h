@@ -8,7 +8,8 @@
 namespace gg {
 
 constexpr int kMaxWorld = 64;
-constexpr int kStatusTimeout = -6;  // GG_ERR_TIMEOUT
+constexpr int kStatusTimeout = -6;    // GG_ERR_TIMEOUT
+constexpr int kStatusNotInHeap = -3;  // GG_ERR_NOT_IN_HEAP (checked build)
 
 // Collectives the gather kernels run.
 constexpr int kModeGather = 0;       // every tile to every member
@@ -39,6 +40,12 @@ bool encode_out_maps(OutMaps *out, const uint64_t *member_out, int W, int64_t M,
 // tile of source src_first + t / (items per source).
 struct GatherArgs {
     const uint64_t *bases;  // device heap-bases table, one entry per heap
+    // The heap layout the table must describe: entry h == heap_lo + h * part_bytes.
+    // Read only by the checked build, which also bounds every raw access by the
+    // extents below.
+    uint64_t heap_lo, part_bytes;
+    int64_t in_ext_b;   // bytes one source's input spans ((rows - 1) * ld_in_b + row_b)
+    int64_t out_ext_b;  // bytes one member's gathered output spans
     int W, rank_start, rank_stride;
     int n_src, src_first;
     const uint8_t *in_abs;  // non-null: the one source's block (any device memory)

@@ -47,7 +47,8 @@ typedef enum {
     GG_OK = 0,
     GG_ERR_INVALID_ARG = -1,  /* bad size, rank, group, pitch or overlap     */
     GG_ERR_ALIGNMENT = -2,    /* pointer/pitch alignment a path requires     */
-    GG_ERR_NOT_IN_HEAP = -3,  /* a symmetric buffer does not fit a partition */
+    GG_ERR_NOT_IN_HEAP = -3,  /* a symmetric buffer does not fit a partition;
+                                 checked build: a device access out of bounds */
     GG_ERR_UNSUPPORTED = -4,  /* valid request this build does not implement */
     GG_ERR_CUDA = -5,         /* a CUDA runtime call failed                  */
     GG_ERR_TIMEOUT = -6       /* device: a bounded wait gave up (status word)*/
@@ -175,6 +176,8 @@ int gg_get_claim_policy(void);
  *   unwritten), GG_ERR_TIMEOUT is stored there (first error wins; the caller
  *   zeroes it).  With NULL it is stored in the library's status word of the
  *   device instead (gg_device_status), so no early stop goes unreported.
+ *   The checked build (gg_checked_build) also stores GG_ERR_NOT_IN_HEAP there
+ *   when a device-side bounds check skips an access.
  *   M == 0 or N == 0 launches nothing and returns GG_OK.
  * Any alignment is accepted: 16-byte aligned pointers and pitches take the
  *   tensor-map or bulk-copy path, others a narrower vector path.  Results
@@ -422,6 +425,36 @@ const char *gg_status_string(gg_status s);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int gg_version(void);
+
+/* ---------------------------------------------------------------------------
+ * gg_checked_build — 1 in the checked build of the library
+ * (libgemm_gather_checked.so), 0 in the release build (libgemm_gather.so).
+ * The pages have no counterpart.
+ *
+ * Both builds export the same calls with the same arguments and results.  The
+ * checked build adds device-side checks to the all-gather, partitioned
+ * all-gather and all-to-all kernels, for finding a wrong heap-bases table or
+ * an indexing fault while developing:
+ *  - every program compares the device heap-bases table with the heap's
+ *    layout (entry h == partition h's address, as gg_heap_bases reports it);
+ *    an entry that differs is reported and not used: the member is reached
+ *    at its partition's address, so the results stay those of a correct
+ *    table;
+ *  - the validated input and output extents must fit inside a partition
+ *    (else the launch reports and returns before its first access);
+ *  - every decoded work item must lie inside the tile grid, and every load
+ *    and store the bulk and vector paths address must lie inside the source
+ *    block or the member's gathered output that the host validated (else
+ *    that access is skipped).
+ * A failed check stores GG_ERR_NOT_IN_HEAP in the launch's status word
+ * (dev_status, or the library's word when it is NULL); first error wins, as
+ * for GG_ERR_TIMEOUT.  The tensor-map paths and the fused kernels address
+ * memory only through tensor maps the host encodes from its own copy of the
+ * bases, clipped to the validated extents by the TMA unit: of these checks
+ * the tensor-map all-gather paths run the table comparison, the extent check
+ * and the item check, the fused kernels none.  The checks cost time: the
+ * checked build is not for measurement. */
+int gg_checked_build(void);
 
 #ifdef __cplusplus
 }

@@ -26,13 +26,27 @@ def declared_functions():
                                  text, flags=re.M)))
 
 
-def test_every_declared_symbol_is_exported():
+BUILDS = {"libgemm_gather.so": 0, "libgemm_gather_checked.so": 1}
+
+
+@pytest.mark.parametrize("name", sorted(BUILDS))
+def test_every_declared_symbol_is_exported(name):
+    """Both builds (release and checked) export every declared call, and
+    gg_checked_build tells them apart (a host-only call)."""
     names = declared_functions()
     assert len(names) >= 14
-    lib = ctypes.CDLL(_lib.LIB_PATH)
+    lib = ctypes.CDLL(os.path.join(os.path.dirname(_lib.LIB_PATH), name))
     for n in names:
         assert hasattr(lib, n), n
     assert sorted(_lib.EXPORTS) == names
+    lib.gg_checked_build.restype = ctypes.c_int
+    assert lib.gg_checked_build() == BUILDS[name]
+    lib.gg_version.restype = ctypes.c_int
+    assert lib.gg_version() == gg.lib.gg_version()
+
+
+def test_loaded_build_follows_the_environment():
+    assert gg.checked_build() == (os.environ.get("GEMM_GATHER_CHECKED", "0") == "1")
 
 
 @pytest.fixture
