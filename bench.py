@@ -772,6 +772,10 @@ def main():
                     "(default: the library's, auto)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.impl == "mine" and os.environ.get("GEMM_GATHER_CHECKED", "0") == "1":
+        # the checked build bounds every access of the gather kernels: a
+        # development build whose times would not describe the library
+        ap.error("GEMM_GATHER_CHECKED=1 loads the checked build, which is not for measurement")
     if args.sweep:
         return run_sweep(args)
     base_g, base_f = PRESETS[args.preset]

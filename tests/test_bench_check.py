@@ -115,3 +115,16 @@ def test_traffic_entries_cover_the_bench_workloads(preset):
     fused = {e["bench_workload"] for e in t["mag2w_kernel" if f.bn == 512 else "mag2_kernel"]}
     assert g.describe() in gather, g.describe()
     assert f.describe() in fused, f.describe()
+
+
+def test_bench_refuses_the_checked_build():
+    """The checked build's bounds checks would make any timing meaningless:
+    bench.py stops before loading it."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, GEMM_GATHER_CHECKED="1")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--steps", "1"], cwd=root,
+                       env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 2 and "not for measurement" in r.stderr, r.stderr
