@@ -1,4 +1,4 @@
-// Host-side TMA tensor maps: the driver's encoder, reached through the
+// Host-side TMA tensor maps: the CUDA driver API's encoder, reached through the
 // runtime's entry-point query (no link against libcuda), and the
 // per-destination output maps of the gathers.
 #include <cuda.h>
