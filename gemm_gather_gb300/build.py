@@ -21,7 +21,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgemm_gather.so")
 LIB_CHECKED = os.path.join(BUILD, "libgemm_gather_checked.so")
-SOURCES = ["gg_api.cu", "ag_kernels.cu", "mag_kernel.cu", "tensor_maps.cu"]
+SOURCES = ["gg_api.cu", "ag_kernels.cu", "mag_kernel.cu", "tensor_maps.cu", "fill_kernel.cu"]
 CHECKED_SOURCES = ["gg_api.cu", "ag_kernels.cu"]  # the units that read GG_CHECKED
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]

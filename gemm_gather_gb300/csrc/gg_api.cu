@@ -628,13 +628,19 @@ gg_status check_fused_path(gg_mag_path path, gg_tile tile, int comm_programs)
     return GG_OK;
 }
 
+// What a validated fused call runs.
+enum FusedWork { kFusedNothing = 0, kFusedMatmul = 1, kFusedZeros = 2 };
+
+// Validation and argument set-up of a fused call.  *work: nothing (M == 0 or
+// N == 0), the matmul kernel (*out_args, *maps), or, for K == 0, the zero
+// fill of the gathered rows (*zeros).  maps and zeros may be NULL (checks).
 gg_status prepare_fused(const gg_heap *heap, int rank, const void *A, int64_t lda, const void *B,
                         int64_t ldb, void *output, int64_t ld_out, int64_t M, int64_t N,
                         int64_t K, gg_dtype dtype, gg_tile tile, int comm_programs,
                         gg_group group, int *dev_status, gg::FusedArgs *out_args,
-                        gg::OutMaps *maps, bool *launch)
+                        gg::OutMaps *maps, gg::ZeroArgs *zeros, FusedWork *work)
 {
-    *launch = false;
+    *work = kFusedNothing;
     int gi = -1;
     gg_status st = check_group(heap, group, rank, &gi);
     if (st != GG_OK)
@@ -656,11 +662,13 @@ gg_status prepare_fused(const gg_heap *heap, int rank, const void *A, int64_t ld
         return fail(GG_ERR_INVALID_ARG, "comm_programs %d outside [1, 65535]", comm_programs);
     if (!output || ((!A || !B) && M > 0 && N > 0 && K > 0))
         return fail(GG_ERR_INVALID_ARG, "A, B and output must be non-NULL");
-    if (M == 0 || N == 0 || K == 0)
+    if (M == 0 || N == 0)
         return ok();
     const uint64_t ua = reinterpret_cast<uint64_t>(A), ub = reinterpret_cast<uint64_t>(B),
                    uo = reinterpret_cast<uint64_t>(output);
-    if ((ua | ub | uo) % 16 != 0 || lda % 8 || ldb % 8 || ld_out % 8 || N % 8)
+    // with K == 0 the operands are never read (every product is the empty sum)
+    const uint64_t operands = K > 0 ? (ua | ub) : 0;
+    if ((operands | uo) % 16 != 0 || (K > 0 && (lda % 8 || ldb % 8)) || ld_out % 8 || N % 8)
         return fail(GG_ERR_ALIGNMENT,
                     "A, B and output must be 16-byte aligned; lda, ldb, ld_out and N multiples "
                     "of 8");
@@ -673,6 +681,23 @@ gg_status prepare_fused(const gg_heap *heap, int rank, const void *A, int64_t ld
     st = symmetric_offset(heap, output, out_ext, "output", &out_off);
     if (st != GG_OK)
         return st;
+    if (K == 0) {
+        // C_r = A_r @ B over an empty k range is the zero matrix: the gathered
+        // rows of the call's sources become zeros in every member's output
+        if (zeros) {
+            for (int q = 0; q < W; ++q)
+                zeros->out[q] =
+                    heap->host_bases[group.rank_start + q * group.rank_stride] + (uint64_t)out_off;
+            zeros->W = W;
+            zeros->src_first = rank == -1 ? 0 : gi;
+            zeros->n_src = rank == -1 ? W : 1;
+            zeros->M = M;
+            zeros->ld_out_b = ld_out * 2;
+            zeros->row_b = N * 2;
+        }
+        *work = kFusedZeros;
+        return ok();
+    }
 
     gg::FusedArgs f{};
     f.W = W;
@@ -735,7 +760,7 @@ gg_status prepare_fused(const gg_heap *heap, int rank, const void *A, int64_t ld
             return fail(GG_ERR_CUDA, "encoding the output tensor maps");
     }
     *out_args = f;
-    *launch = true;
+    *work = kFusedMatmul;
     return ok();
 }
 
@@ -754,11 +779,17 @@ gg_status gg_matmul_all_gather_path(const gg_heap *heap, int rank, const void *A
         return st;
     gg::FusedArgs f;
     static thread_local gg::OutMaps maps;
-    bool launch = false;
+    gg::ZeroArgs zeros;
+    FusedWork work = kFusedNothing;
     st = prepare_fused(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype, tile,
-                       comm_programs, group, dev_status, &f, &maps, &launch);
-    if (st != GG_OK || !launch)
+                       comm_programs, group, dev_status, &f, &maps, &zeros, &work);
+    if (st != GG_OK || work == kFusedNothing)
         return st;
+    if (work == kFusedZeros) {
+        const cudaError_t e =
+            gg::launch_zero_rows(zeros, comm_programs, reinterpret_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? ok() : cuda_fail(e, "launching the zero fill (K == 0)");
+    }
     st = resolve_status(&f.status);
     if (st != GG_OK)
         return st;
@@ -790,9 +821,9 @@ gg_status gg_matmul_all_gather_check(const gg_heap *heap, int rank, const void *
     if (st != GG_OK)
         return st;
     gg::FusedArgs f;
-    bool launch = false;
+    FusedWork work = kFusedNothing;
     return prepare_fused(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype, tile,
-                         comm_programs, group, nullptr, &f, nullptr, &launch);
+                         comm_programs, group, nullptr, &f, nullptr, nullptr, &work);
 }
 
 gg_status gg_matmul_all_gather_plan(const gg_heap *heap, int rank, const void *A, int64_t lda,
@@ -807,10 +838,10 @@ gg_status gg_matmul_all_gather_plan(const gg_heap *heap, int rank, const void *A
     if (st != GG_OK)
         return st;
     gg::FusedArgs f;
-    bool launch = false;
+    FusedWork work = kFusedNothing;
     st = prepare_fused(heap, rank, A, lda, B, ldb, output, ld_out, M, N, K, dtype, tile,
-                       comm_programs, group, nullptr, &f, nullptr, &launch);
-    if (st == GG_OK && launch && chosen)
+                       comm_programs, group, nullptr, &f, nullptr, nullptr, &work);
+    if (st == GG_OK && work == kFusedMatmul && chosen)
         *chosen = (gg_mag_path)gg::fused_variant(comm_programs, (int)path);
     return st;
 }

@@ -121,4 +121,17 @@ inline int fused_variant(int programs, int requested)
 cudaError_t launch_matmul_all_gather(const FusedArgs &a, const OutMaps &out, int programs,
                                      int variant, cudaStream_t s, const char **why);
 
+// The fused call with K == 0: every product is the zero matrix, so the rows of
+// sources [src_first, src_first + n_src) in every member's gathered output
+// are filled with zeros (fill_kernel.cu).  Row pitch and row length are whole
+// 16-byte units and the outputs 16-byte aligned.
+struct ZeroArgs {
+    uint64_t out[kMaxWorld];  // gathered output of member d (host-side bases + offset)
+    int W;
+    int src_first, n_src;
+    int64_t M;                // rows per source block
+    int64_t ld_out_b, row_b;  // row pitch and row length in bytes
+};
+cudaError_t launch_zero_rows(const ZeroArgs &z, int programs, cudaStream_t s);
+
 }  // namespace gg

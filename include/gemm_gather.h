@@ -346,8 +346,12 @@ gg_status gg_collective_check(gg_collective kind, const gg_heap *heap, int rank,
  *   each pair on twice the tile's rows); a single program runs alone on
  *   128 x 256 tiles.
  * dev_status: as for gg_all_gather (NULL: the library's status word).
- * M, N or K == 0: nothing is launched, GG_OK (with K == 0 nothing is
- *   written either).
+ * M or N == 0: nothing is launched, GG_OK.
+ * K == 0: every product is the empty sum, the zero matrix: the call writes
+ *   zeros into the gathered rows of its sources (all of them for rank == -1)
+ *   in every member's output, padding columns untouched.  A and B are not
+ *   read and may be NULL; the output is validated as above.  No matmul
+ *   kernel runs (a plain fill).
  * ------------------------------------------------------------------------- */
 gg_status gg_matmul_all_gather(const gg_heap *heap, int rank, const void *A, int64_t lda,
                                const void *B, int64_t ldb, void *output, int64_t ld_out,
@@ -372,7 +376,8 @@ gg_status gg_matmul_all_gather_path(const gg_heap *heap, int rank, const void *A
 /* Validate a gg_matmul_all_gather_path call exactly as the launching call
  * does and launch nothing; *chosen (nullable) receives the kernel variant a
  * launch would run: GG_MAG_1SM (a single program, or asked for) or
- * GG_MAG_2SM; GG_MAG_AUTO when there is nothing to launch. */
+ * GG_MAG_2SM; GG_MAG_AUTO when no matmul kernel would run (M or N == 0:
+ * nothing; K == 0: the zero fill). */
 gg_status gg_matmul_all_gather_plan(const gg_heap *heap, int rank, const void *A, int64_t lda,
                                     const void *B, int64_t ldb, void *output, int64_t ld_out,
                                     int64_t M, int64_t N, int64_t K, gg_dtype dtype,

@@ -370,6 +370,33 @@ def pin_fused_integers(o) -> None:
         assert np.array_equal(heap[~mask], before[~mask])
 
 
+def pin_fused_empty_contraction(o) -> None:
+    """K = 0: every product is the empty sum, +0 (numpy's matmul of an M x 0 by
+    a 0 x N matrix agrees), so every member's gathered output holds all-zero
+    bit patterns in its data columns and nothing else changes."""
+    for fmt in (0, 1):
+        H, group, M, N = 5, (0, 2, 3), 7, 24
+        W = group[2]
+        members = _members(group)
+        lay = hi.make_layout(H, W, M, N, 2, ld_in=8, ld_out=N + 8)
+        heap = hi.sentinel_heap(lay)
+        before = heap.copy()
+        A0 = np.zeros((M, 0), dtype=np.float64)
+        B = np.zeros((0, N), dtype=np.uint16)  # 0 x N, row pitch N
+        prods = o.matmul_all_gather(heap, lay.part_bytes, lay.in_off, lay.ld_in, B, lay.out_off,
+                                    lay.ld_out, M, N, 0, fmt, group)
+        for i in range(W):
+            assert np.array_equal(prods[i], A0 @ np.zeros((0, N))), (fmt, i)
+            assert not np.signbit(prods[i]).any()
+        for d in members:
+            out = hi.get_block(heap, lay, d, lay.out_off, W * M, lay.ld_out, N, np.uint16)
+            assert not out.any(), (fmt, d)
+        mask = hi.output_mask(lay, members)
+        assert np.array_equal(heap[~mask], before[~mask])
+        # the padding columns inside the output region keep their bytes too
+        assert hi.output_mask(lay, members).sum() == W * W * M * N * 2
+
+
 ALL_PINS = [
     pin_group_index,
     pin_gather_packed,
@@ -385,4 +412,5 @@ ALL_PINS = [
     pin_matmul_closed_forms,
     pin_matmul_row_sample,
     pin_fused_integers,
+    pin_fused_empty_contraction,
 ]

@@ -207,6 +207,7 @@ def test_fused_plan_variants(heap):
     assert plan(heap, tile=gg.FUSED_TILE_WIDE) == "2sm"
     assert plan(heap, tile=gg.FUSED_TILE_WIDE, path="2sm", N=256) == "2sm"
     assert plan(heap, M=0) == "none"
+    assert plan(heap, K=0) == "none"   # no matmul kernel: the output is filled with zeros
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -220,6 +221,20 @@ def test_fused_plan_rejects(heap, kw, status):
     with pytest.raises(gg.GGError) as e:
         plan(heap, **kw)
     assert e.value.status == status, str(e.value)
+
+
+def test_fused_empty_contraction_validates_the_output_only(heap):
+    """K == 0: C_r is the zero matrix; A and B are never read (NULL or unaligned
+    is fine), but the output must still be an aligned buffer inside the heap."""
+    mag(heap, K=0, A=None, B=None)
+    mag(heap, K=0, A=BASE + 4100, lda=3)
+    for kw, status in [(dict(output=BASE + (4 << 20) + 8), _lib.GG_ERR_ALIGNMENT),
+                       (dict(output=BASE + PART - 4096), _lib.GG_ERR_NOT_IN_HEAP),
+                       (dict(N=500, ldb=512, ld_out=512), _lib.GG_ERR_ALIGNMENT),
+                       (dict(ld_out=8196), _lib.GG_ERR_ALIGNMENT)]:
+        with pytest.raises(gg.GGError) as e:
+            mag(heap, K=0, **kw)
+        assert e.value.status == status, (kw, str(e.value))
 
 
 def test_fused_valid_calls(heap):

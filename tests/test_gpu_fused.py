@@ -153,12 +153,34 @@ def test_single_rank_launches(oracle, dtype, path):
     run_fused(oracle, 6, (1, 2, 3), 96, 256, 320, dtype, 3, "normal", mode="ranks", path=path)
 
 
-def test_zero_k_writes_nothing():
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("mode", ["group", "ranks"])
+def test_empty_contraction_gathers_zero_blocks(oracle, mode, dtype, path):
+    """K == 0: C_r is the empty sum, the zero matrix; every member's gathered
+    rows become zeros (padding columns untouched), exactly as the oracle's
+    definition gives.  A and B are not read: B is passed as NULL."""
     import gemm_gather_gb300 as gg
-    lay = hi.make_layout(2, 2, 128, 256, 2, ld_in=64)
+    kpath, tile = kernel_args(path)
+    H, group, M, N = 5, (1, 1, 3), 130, 264
+    start, stride, W = group
+    members = [start + i * stride for i in range(W)]
+    lay = hi.make_layout(H, W, M, N, 2, ld_in=8, ld_out=N + 8)
     host = hi.sentinel_heap(lay)
     sh = device_heap(lay, host)
-    B = torch.zeros((1, 256), dtype=torch.float16, device="cuda")
-    gg.matmul_all_gather(sh.heap, -1, sh.ptr(0, lay.in_off), 64, B, 256, sh.ptr(0, lay.out_off),
-                         256, 128, 256, 0, torch.float16, gg.FUSED_TILE, 4, (0, 1, 2))
-    assert np.array_equal(download(sh), host)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    programs = 1 if path == "1sm" else 6
+    if mode == "group":
+        gg.matmul_all_gather(sh.heap, -1, sh.ptr(start, lay.in_off), 8, None, N,
+                             sh.ptr(start, lay.out_off), lay.ld_out, M, N, 0, dtype, tile,
+                             programs, group, status=status, path=kpath)
+    else:
+        for h in members:
+            gg.matmul_all_gather(sh.heap, h, sh.ptr(h, lay.in_off), 8, None, N,
+                                 sh.ptr(h, lay.out_off), lay.ld_out, M, N, 0, dtype, tile,
+                                 programs, group, status=status, path=kpath)
+    got = download(sh)
+    assert int(status.item()) == 0
+    oracle.matmul_all_gather(host, lay.part_bytes, lay.in_off, 8, np.zeros((0, N), np.uint16),
+                             lay.out_off, lay.ld_out, M, N, 0, FMT[dtype], group)
+    assert np.array_equal(got, host), first_diff(got, host, lay)
