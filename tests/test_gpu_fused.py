@@ -184,3 +184,87 @@ def test_empty_contraction_gathers_zero_blocks(oracle, mode, dtype, path):
     oracle.matmul_all_gather(host, lay.part_bytes, lay.in_off, 8, np.zeros((0, N), np.uint16),
                              lay.out_off, lay.ld_out, M, N, 0, FMT[dtype], group)
     assert np.array_equal(got, host), first_diff(got, host, lay)
+
+
+def _fused_custom(oracle, A, B, dtype, path, group=(0, 1, 2)):
+    """Run the group launch on the given operands (A: {member: M x K}, B: K x N)
+    and return (device heap, oracle heap, layout, members)."""
+    import gemm_gather_gb300 as gg
+    kpath, tile = kernel_args(path)
+    start, stride, W = group
+    members = [start + i * stride for i in range(W)]
+    M, K = A[members[0]].shape
+    N = B.shape[1]
+    H = members[-1] + 1
+    lay = hi.make_layout(H, W, M, N, 2, ld_in=K, ld_out=N)
+    host = hi.sentinel_heap(lay)
+    for h in members:
+        hi.put_block(host, lay, h, _bits(A[h]), lay.in_off, K)
+    sh = device_heap(lay, host)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gg.matmul_all_gather(sh.heap, -1, sh.ptr(start, lay.in_off), K, B.to("cuda"), N,
+                         sh.ptr(start, lay.out_off), N, M, N, K, dtype, tile,
+                         1 if path == "1sm" else 4, group, status=status, path=kpath)
+    got = download(sh)
+    assert int(status.item()) == 0
+    oracle.matmul_all_gather(host, lay.part_bytes, lay.in_off, K, _bits(B), lay.out_off, N, M, N,
+                             K, FMT[dtype], group)
+    return got, host, lay, members
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+def test_overflowing_sums_round_like_the_oracle(oracle, dtype, path):
+    """A in {-256, 0, 256} and B in {-256, -1, 0, 1, 256}: every product is 0,
+    +-256 or +-65536 and every f32 partial sum an exact multiple of 256 below
+    2^24, so the products are exact whatever order the sums take.  Sums of
+    65536 or more pass binary16's largest finite value (65504): the f16
+    outputs hold +-inf there, as round-to-nearest-even gives; the whole heap
+    must match the oracle bit for bit."""
+    g = gg_inputs.generator(21)
+    M, N, K = 160, 512, 64
+
+    def draw(shape, vals):
+        v = torch.tensor(vals)
+        return v[torch.randint(0, len(vals), shape, generator=g)].to(dtype)
+
+    A = {h: draw((M, K), [-256.0, 0.0, 256.0]) for h in (0, 1)}
+    B = draw((K, N), [-256.0, -1.0, 0.0, 1.0, 256.0])
+    got, host, lay, _ = _fused_custom(oracle, A, B, dtype, path)
+    if dtype == torch.float16:
+        out = hi.get_block(host, lay, 0, lay.out_off, 2 * M, N, N, np.uint16)
+        assert ((out & 0x7FFF) == 0x7C00).sum() > 1000  # the case reaches overflow
+    assert np.array_equal(got, host), first_diff(got, host, lay)
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+def test_non_finite_operands_propagate(oracle, dtype, path):
+    """+-inf and NaN in A: inf * 0 and inf - inf give NaN, inf * x gives inf,
+    NaN spreads along its row.  NaN has no unique encoding, so the test
+    compares which outputs are NaN and every other output bit for bit (inf
+    signs included); the W copies must be identical and nothing outside the
+    outputs may change."""
+    g = gg_inputs.generator(22)
+    M, N, K = 128, 256, 64
+    A = {}
+    for h in (0, 1):
+        a = gg_inputs.integers((M, K), -2, 2, dtype, g)
+        a[3, 5] = float("inf")
+        a[9, 0] = float("-inf")
+        a[17, 2], a[17, 40] = float("inf"), float("-inf")
+        a[33, 7] = float("nan")
+        A[h] = a
+    B = gg_inputs.integers((K, N), -2, 2, dtype, g)
+    B[5, :8] = 0            # inf * 0 = NaN in row 3's first columns
+    got, host, lay, members = _fused_custom(oracle, A, B, dtype, path)
+    mask = hi.output_mask(lay, members)
+    assert np.array_equal(got[~mask], host[~mask]), "bytes outside the outputs changed"
+    outs = [hi.get_block(got, lay, d, lay.out_off, 2 * M, N, N, np.uint16) for d in members]
+    assert np.array_equal(outs[0], outs[1]), "destination copies differ"
+    ref = hi.get_block(host, lay, 0, lay.out_off, 2 * M, N, N, np.uint16)
+    exp_mask, man_mask = (0x7C00, 0x03FF) if dtype == torch.float16 else (0x7F80, 0x007F)
+    nan_got = ((outs[0] & exp_mask) == exp_mask) & ((outs[0] & man_mask) != 0)
+    nan_ref = ((ref & exp_mask) == exp_mask) & ((ref & man_mask) != 0)
+    assert nan_ref.sum() >= 2 * N and np.array_equal(nan_got, nan_ref)
+    assert np.array_equal(outs[0][~nan_ref], ref[~nan_ref])
