@@ -835,6 +835,32 @@ constexpr int kOffShared = kOffEpi + kEpiWarps * kBox;
 constexpr int kSmemBytes = kOffShared + (int)sizeof(FusedShared) + 1024;
 static_assert(kSmemBytes <= 232448, "at most 227 KB of dynamic shared memory per CTA");
 static_assert(kStages <= kMaxStages, "ring barriers");
+
+// Work units.  A pair tile is one unit, except in a last wave that is at
+// most half full (total mod pairs <= pairs / 2): its tiles are split into
+// their two N halves (256 x 256 each, one MMA per K step), so that twice as
+// many pairs share the tail and the kernel ends half a tile earlier.  Units
+// [0, full) are whole tiles; unit full + 2j + h is half h of tile full + j.
+struct Unit {
+    int64_t t;   // pair tile
+    int h0, nh;  // N halves computed: [h0, h0 + nh)
+};
+
+__device__ __forceinline__ Unit unit_of(int64_t u, int64_t full)
+{
+    Unit w;
+    if (u < full) {
+        w.t = u;
+        w.h0 = 0;
+        w.nh = 2;
+    } else {
+        const int64_t v = u - full;
+        w.t = full + v / 2;
+        w.h0 = (int)(v & 1);
+        w.nh = 1;
+    }
+    return w;
+}
 }  // namespace wide
 
 __device__ __forceinline__ void magw_body(const CUtensorMap &map_a, const CUtensorMap &map_b,
@@ -856,6 +882,9 @@ __device__ __forceinline__ void magw_body(const CUtensorMap &map_a, const CUtens
     const int tiles_m = (int)((a.M + wide::kTileM - 1) / wide::kTileM);
     const int tiles_n = (int)((a.N + wide::kTileN - 1) / wide::kTileN);
     const int64_t total = (int64_t)a.n_src * tiles_m * tiles_n;
+    const int64_t rem = total % nunits;
+    const int64_t full = rem != 0 && 2 * rem <= nunits ? total - rem : total;
+    const int64_t units = total + (total - full);  // a split tile is two units
     const int num_kb = (int)((a.K + wide::kBK - 1) / wide::kBK);
 
     if (threadIdx.x == 0) {
@@ -888,13 +917,15 @@ __device__ __forceinline__ void magw_body(const CUtensorMap &map_a, const CUtens
         // ===================== producer =====================================
         const uint64_t pol_a = ptx::policy_evict_normal();
         const uint64_t pol_b = ptx::policy_evict_last();
-        constexpr uint32_t kTx = 2 * (wide::kAStage + wide::kBStage);  // both CTAs
         int stage = 0;
         uint32_t phase = 0;
         int64_t issued = 0;
         bool ok = true;
-        for (int64_t t = unit; t < total && ok; t += nunits) {
-            const TileCoord c = tile_coord(a, t, tiles_m, tiles_n);
+        for (int64_t u = unit; u < units && ok; u += nunits) {
+            const wide::Unit w = wide::unit_of(u, full);
+            const TileCoord c = tile_coord(a, w.t, tiles_m, tiles_n);
+            // bytes of one stage, both CTAs: A and the unit's halves of B
+            const uint32_t tx = 2u * (uint32_t)(wide::kAStage + w.nh * wide::kBHalf);
             const int h_coord = a.a_abs ? 0 : c.h;
             const int row0 = c.tm * wide::kTileM + (int)rank * BM;
             const int colh0 = c.tn * wide::kTileN + (int)rank * (BN / 2);  // N half 0
@@ -910,12 +941,15 @@ __device__ __forceinline__ void magw_body(const CUtensorMap &map_a, const CUtens
                     const uint32_t local_full = ptx::smem_addr(&sh.full[stage]);
                     const uint32_t bar = map_to_rank(local_full, 0);
                     if (leader)
-                        ptx::mbar_arrive_expect_tx(local_full, kTx);
+                        ptx::mbar_arrive_expect_tx(local_full, tx);
                     const uint32_t sa = base + wide::kOffA + stage * wide::kAStage;
                     const uint32_t sb = base + wide::kOffB + stage * wide::kBStage;
                     tma_load_3d<2>(sa, &map_a, kq * wide::kBK, row0, h_coord, bar, pol_a);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (hh >= w.nh)
+                            break;
+                        const int h = w.h0 + hh;
                         const int col0 = colh0 + h * BN;
                         if (a.b_boxes3d) {
                             tma_load_3d<2>(sb + h * wide::kBHalf, &map_b, 0, kq * wide::kBK,
@@ -959,7 +993,8 @@ __device__ __forceinline__ void magw_body(const CUtensorMap &map_a, const CUtens
         int64_t lt = 0;
         bool issued_any = false;
         bool ok = true;
-        for (int64_t t = unit; leader && t < total && ok; t += nunits, ++lt) {
+        for (int64_t u = unit; leader && u < units && ok; u += nunits, ++lt) {
+            const wide::Unit w = wide::unit_of(u, full);
             // the epilogue has copied the previous tile's accumulator out of TMEM
             const bool free_acc = role_wait(ptx::smem_addr(&sh.tmem_empty[0]),
                                             (uint32_t)(lt & 1) ^ 1u, a.wait_limit_ns, abort_flag);
@@ -983,7 +1018,10 @@ __device__ __forceinline__ void magw_body(const CUtensorMap &map_a, const CUtens
                     for (int k = 0; k < wide::kBK / UK; ++k) {
                         const uint64_t ad = smem_desc(sa + (uint32_t)(k * UK * 2), 16, 1024);
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
+                        for (int hh = 0; hh < 2; ++hh) {
+                            if (hh >= w.nh)
+                                break;
+                            const int h = w.h0 + hh;
                             const uint64_t bd = smem_desc(
                                 sb + (uint32_t)(h * wide::kBHalf + k * (UK * 128)), wide::kBBox, 1024);
                             mma_f16<2>(tmem + (uint32_t)(h * BN), ad, bd, idesc,
@@ -1029,8 +1067,9 @@ __device__ __forceinline__ void magw_body(const CUtensorMap &map_a, const CUtens
         int64_t lt = 0;
         bool ok = true;
         uint64_t prev_ready = ptx::globaltimer();
-        for (int64_t t = unit; t < total; t += nunits, ++lt) {
-            const TileCoord c = tile_coord(a, t, tiles_m, tiles_n);
+        for (int64_t u = unit; u < units; u += nunits, ++lt) {
+            const wide::Unit w = wide::unit_of(u, full);
+            const TileCoord c = tile_coord(a, w.t, tiles_m, tiles_n);
             const bool got = role_wait(ptx::smem_addr(&sh.tmem_full[0]), (uint32_t)(lt & 1),
                                        a.wait_limit_ns, abort_flag);
             if (!__all_sync(0xffffffffu, got)) {
@@ -1038,12 +1077,19 @@ __device__ __forceinline__ void magw_body(const CUtensorMap &map_a, const CUtens
                 break;
             }
             tc_fence_after();
+            if (half < w.h0 || half >= w.h0 + w.nh) {
+                // a half tile without this warp's columns: nothing to copy
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive_cluster(map_to_rank(ptx::smem_addr(&sh.tmem_empty[0]), 0));
+                continue;
+            }
             const uint64_t t_ready = ptx::globaltimer();
             uint64_t period = t_ready - prev_ready;
             period = period > kPaceMaxPeriodNs ? kPaceMaxPeriodNs : period;
             prev_ready = t_ready;
             const uint64_t slot =
-                t + nunits < total ? period * kPacePct / 100u / (uint64_t)(kBoxes * a.W) : 0;
+                u + nunits < units ? period * kPacePct / 100u / (uint64_t)(kBoxes * a.W) : 0;
             // the whole accumulator slice of this warp, as packed 16-bit pairs
             // (16 columns per load keeps it within the registers, no spills)
             uint32_t pk[kBoxes * 32];

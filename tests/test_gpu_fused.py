@@ -146,6 +146,26 @@ def test_random_operands_within_tolerance(oracle, shape, dtype, path):
     run_fused(oracle, 3, (0, 1, 3), M, N, K, dtype, 7, "normal", path=path)
 
 
+# (H, group, M, N, K, programs): the 128 x 512 kernel's last wave is at most
+# half full, so its pair tiles run as two 256 x 256 halves on twice as many pairs
+TAIL_CASES = [
+    (3, (0, 1, 3), 256, 1024, 256, 8),     # 6 tiles on 4 pairs: 2 split
+    (5, (0, 1, 5), 300, 776, 200, 18),     # 20 tiles on 9 pairs: 2 split, ragged M, N, K
+    (8, (1, 2, 3), 100, 520, 64, 10),      # 6 tiles on 5 pairs: 1 split, its half 1 empty
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
+@pytest.mark.parametrize("case", TAIL_CASES, ids=lambda c: f"H{c[0]}g{c[1]}_{c[2]}x{c[3]}x{c[4]}p{c[5]}")
+def test_wide_tail_half_tiles_bit_exact(oracle, case, dtype):
+    H, group, M, N, K, programs = case
+    total = group[2] * -(-M // 256) * -(-N // 512)
+    pairs = min(programs // 2, total)
+    assert 0 < total % pairs and 2 * (total % pairs) <= pairs  # the tail is split
+    run_fused(oracle, H, group, M, N, K, dtype, programs, "int", path="wide")
+    run_fused(oracle, H, group, M, N, K, dtype, programs, "normal", path="wide", seed=1)
+
+
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16], ids=["f16", "bf16"])
 def test_single_rank_launches(oracle, dtype, path):
