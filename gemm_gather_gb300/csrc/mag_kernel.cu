@@ -5,8 +5,9 @@
 // C_r = A_r @ B for every source r of the launch.  Persistent CTAs, one per
 // SM.  Three kernels, chosen by the caller's tile and path:
 //   * mag2w (128 x 512 CTA tile): CTA pairs (clusters of 2) on 256 x 512
-//     tiles, two tcgen05.mma.cta_group::2 per K step sharing the A stage; see
-//     the "wide pair tiles" section below for how it differs from mag2;
+//     tiles, two tcgen05.mma.cta_group::2 per K step sharing the A stage; a
+//     last wave at most half full runs as 256 x 256 half tiles (wide::Unit);
+//     see the "wide pair tiles" section below for how it differs from mag2;
 //   * mag2 (128 x 256 CTA tile): CTA pairs on 256 x 256 tiles;
 //   * mag1 (128 x 256 CTA tile, one CTA): 128 x 256 tiles.
 // Tiles are taken in column groups, so that a wave of tiles reads few
