@@ -382,8 +382,8 @@ def run_reference(args, peaks, peak_src, g, f):
         "metric": METRIC, "value": value, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": config_block(peaks, peak_src, g, f),
+        "vs_baseline": None, "dtype": "+".join(sorted({c.dtype for c in (g, f) if c is not None})),
+        "data": "synthetic", "config": config_block(peaks, peak_src, g, f),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": (f"each step: oracle gather on {rows_g} rows per rank and "
                                     f"fused path on {rows_f} rows per rank")},
