@@ -183,3 +183,52 @@ def test_policy_keeps_fixed_shares(oracle, policy):
     assert _counter(sh, 0) == 0
     oracle.all_gather(host, lay.part_bytes, lay.in_off, N, lay.out_off, N, M, N, es, group)
     assert np.array_equal(got, host), first_diff(got, host, lay)
+
+
+def test_concurrent_launches_on_several_streams(oracle):
+    """Five launches in flight at once on five streams, into disjoint output
+    regions of one heap: two claiming tensor-map all-gathers (each takes its
+    own workspace slot), a grouped bulk all-gather, a partitioned all-gather on
+    the vector path and a claiming all-to-all.  Each region must hold the
+    oracle's result and nothing else may change, as if the launches had run
+    one after another; every status word stays 0."""
+    import gemm_gather_gb300 as gg
+    H, group, M, N, es, tile = 4, (0, 1, 4), 256, 2048, 2, (8, 256)
+    W = group[2]
+    base = hi.make_layout(H, W, W * M, N, es)            # inputs hold W*M rows (all-to-all)
+    region = -(-(W * M * N * es + hi.GUARD) // 4096) * 4096   # one gathered output + guard
+    part = base.out_off + 5 * region
+    lay = hi.Layout(H, part, base.in_off, N, base.out_off, N, M, N, W, es)
+    host = np.full(H * part, gg_inputs.SENTINEL_BYTE, dtype=np.uint8)
+    for h in range(H):
+        hi.put_block(host, lay, h, gg_inputs.index_coded(h * 97 + 11, W * M, N, es).numpy(),
+                     lay.in_off, N)
+    sh = device_heap(lay, host, workspace_slots=8)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(5)]
+    status = torch.zeros(5, dtype=torch.int32, device="cuda")
+    out = [lay.out_off + j * region for j in range(5)]
+    inp = sh.ptr(0, lay.in_off)
+    calls = [
+        lambda s, st: gg.all_gather(sh.heap, -1, inp, N, sh.ptr(0, out[0]), N, M, N, DT[es], tile,
+                                    3, group, status=st, stream=s, path="tma"),
+        lambda s, st: gg.all_gather(sh.heap, -1, inp, N, sh.ptr(0, out[1]), N, M, N, DT[es], tile,
+                                    5, group, status=st, stream=s, path="tma"),
+        lambda s, st: gg.all_gather_grouped(sh.heap, -1, inp, N, sh.ptr(0, out[2]), N, M, N,
+                                            DT[es], tile, 4, group, 2, status=st, stream=s,
+                                            path="bulk"),
+        lambda s, st: gg.all_gather_partitioned(sh.heap, -1, inp, N, sh.ptr(0, out[3]), N, M, N,
+                                                DT[es], (16, 128), 8, group, status=st, stream=s,
+                                                path="vector"),
+        lambda s, st: gg.all_to_all(sh.heap, -1, inp, N, sh.ptr(0, out[4]), N, M, N, DT[es],
+                                    tile, 3, group, status=st, stream=s, path="tma"),
+    ]
+    for s, call, st in zip(streams, calls, status):
+        call(s, st)
+    got = download(sh)
+    assert status.tolist() == [0] * 5
+    for j in range(4):
+        oracle.all_gather(host, part, lay.in_off, N, out[j], N, M, N, es, group)
+    oracle.all_to_all(host, part, lay.in_off, N, out[4], N, M, N, es, group)
+    assert np.array_equal(got, host), first_diff(got, host, lay)
+    assert _counter(sh, 0) > 0 and _counter(sh, 1) > 0 and _counter(sh, 2) > 0
