@@ -177,6 +177,19 @@ def source_sha(name: str) -> str:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
+# Dense f16/bf16 tensor-core FLOPs per SM per cycle (tcgen05, nominal).
+TC_FLOP_PER_SM_CYCLE = 8192
+
+
+def kernel_clock(rec):
+    """The SM clock a traced launch ran at (gg_trace_read), or None if no
+    traced launch wrote the record."""
+    if not rec or not rec.get("sm_mhz"):
+        return None
+    return {"sm_mhz": rec["sm_mhz"], "cycles": rec["cycles"], "ns": rec["ns"],
+            "source": "the launch's first CTA: clock64 and %globaltimer at its start and end"}
+
+
 def traffic_for(kernel: str, src: str, workload: str):
     """Per-launch DRAM bytes of `kernel` on `workload` from the committed ncu
     summary, or None when no entry covers that workload or the kernel source
@@ -843,6 +856,9 @@ def main():
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    # each kernel's first CTA records its start/end wall time and SM cycles (four
+    # 8-byte stores per launch): the clock the kernel itself ran at
+    gg.set_trace(True)
     for _ in range(args.warmup):
         step()
     barrier()
@@ -859,11 +875,17 @@ def main():
     t_end.record(stream)
     barrier()
     clk = clocks.stop() if clocks else None
+    trace = gg.trace_read(stream)  # the last timed launch of each kernel
+    gg.set_trace(False)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} after the timed steps")
     elapsed_ms = t_start.elapsed_time(t_end)
-    g_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs) if g else 0.0
-    f_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs) if f else 0.0
+    g_all = [e[0].elapsed_time(e[1]) for e in evs] if g else [0.0]
+    f_all = [e[1].elapsed_time(e[2]) for e in evs] if f else [0.0]
+    g_ms, f_ms = statistics.mean(g_all), statistics.mean(f_all)
+
+    def spread(xs):  # per-launch statistics of one kernel over the timed steps
+        return {"median": statistics.median(xs), "min": min(xs), "max": max(xs)}
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
     ms_step = elapsed_ms / args.steps
 
@@ -1047,7 +1069,9 @@ def main():
     if g:
         g_gbs = gather_bytes(g) / (g_ms * 1e-3) / 1e9
         kname = {"vector": "ag_vec_kernel", "bulk": "ag_bulk_kernel"}.get(g.path, "ag_tma_kernel")
-        kernels["all_gather"] = {"kernel": kname, "ms": g_ms, "GB/s": g_gbs,
+        kernels["all_gather"] = {"kernel": kname, "ms": g_ms, "ms_per_launch": spread(g_all),
+                                 "clock": kernel_clock(trace["all_gather"]),
+                                 "GB/s": g_gbs,
                                  "roofline_ms": 1e3 * t_rg, "frac": g_gbs / hbm_peak,
                                  "bound": "hbm", "algorithmic_bytes": gather_bytes(g),
                                  "traffic": traffic_for(kname, "ag_kernels.cu", g.describe())}
@@ -1059,7 +1083,15 @@ def main():
                                            (f.start, f.stride, f.W), f.path)
         fk = "mag1_kernel" if chosen == "1sm" else ("mag2w_kernel" if f.bn == 512 else
                                                      "mag2_kernel")
-        kernels["matmul_all_gather"] = {"kernel": fk, "ms": f_ms, "TFLOP/s": f_tfs,
+        fclk = kernel_clock(trace["matmul_all_gather"])
+        if fclk:
+            # work per SM cycle against the tensor pipes' nominal dense rate
+            fclk["per_clock_frac"] = fused_flops(f) / (fclk["cycles"] * sms * TC_FLOP_PER_SM_CYCLE)
+            fclk["per_clock_note"] = (f"FLOPs / (SM cycles of the traced launch x {sms} SMs x "
+                                      f"{TC_FLOP_PER_SM_CYCLE} dense f16 FLOP per SM cycle)")
+        kernels["matmul_all_gather"] = {"kernel": fk, "ms": f_ms, "ms_per_launch": spread(f_all),
+                                        "clock": fclk,
+                                        "TFLOP/s": f_tfs,
                                         "roofline_ms": 1e3 * t_rf, "frac": f_tfs / tc_peak,
                                         "bound": "tensor", "algorithmic_flops": fused_flops(f),
                                         "algorithmic_bytes": fused_bytes(f),

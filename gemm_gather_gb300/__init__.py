@@ -31,7 +31,7 @@ __all__ = [
     "set_claim_policy",
     "get_claim_policy", "CLAIM_POLICIES", "set_wait_limit_ns",
     "get_wait_limit_ns", "debug_inject_stall", "device_status", "clear_device_status",
-    "checked_build", "SymmetricHeap", "Heap", "GGError", "DTYPE_CODES", "PATHS",
+    "checked_build", "set_trace", "trace_read", "SymmetricHeap", "Heap", "GGError", "DTYPE_CODES", "PATHS",
     "FUSED_TILE", "FUSED_TILE_WIDE", "FUSED_PATHS",
 ]
 
@@ -274,6 +274,29 @@ def device_status(stream=None) -> int:
 def clear_device_status(stream=None) -> None:
     """Reset the library's status word of the current device to 0 (on ``stream``)."""
     check(lib.gg_clear_device_status(_stream(stream)))
+
+
+def set_trace(enable: bool) -> None:
+    """Launches after this call record their first CTA's start and end wall time
+    and SM cycle counter (gg_set_trace); False stops it."""
+    check(lib.gg_set_trace(1 if enable else 0))
+
+
+def trace_read(stream=None) -> dict:
+    """The last traced launch of each kernel family, after ``stream``'s queued
+    work: {"all_gather": {...}, "matmul_all_gather": {...}}, each with the raw
+    record, its wall time (ns), SM cycles and clock (MHz; None if unwritten)."""
+    from ._lib import TraceRecord
+    rec = {k: TraceRecord() for k in ("all_gather", "matmul_all_gather")}
+    check(lib.gg_trace_read(_stream(stream), ctypes.byref(rec["all_gather"]),
+                            ctypes.byref(rec["matmul_all_gather"])))
+    out = {}
+    for k, r in rec.items():
+        ns, cyc = r.end_ns - r.start_ns, r.end_cycles - r.start_cycles
+        out[k] = {"start_ns": r.start_ns, "end_ns": r.end_ns, "start_cycles": r.start_cycles,
+                  "end_cycles": r.end_cycles, "ns": ns, "cycles": cyc,
+                  "sm_mhz": cyc * 1e3 / ns if r.end_ns > r.start_ns else None}
+    return out
 
 
 def checked_build() -> bool:

@@ -47,12 +47,18 @@ EXPORTS = (
     "gg_set_claim_policy", "gg_get_claim_policy",
     "gg_set_wait_limit_ns", "gg_get_wait_limit_ns", "gg_debug_inject_stall",
     "gg_device_status", "gg_clear_device_status",
+    "gg_set_trace", "gg_trace_read",
     "gg_last_error", "gg_status_string", "gg_version", "gg_checked_build",
 )
 
 
 class Tile(ctypes.Structure):
     _fields_ = [("block_m", ctypes.c_int), ("block_n", ctypes.c_int)]
+
+
+class TraceRecord(ctypes.Structure):
+    _fields_ = [("start_ns", ctypes.c_uint64), ("start_cycles", ctypes.c_uint64),
+                ("end_ns", ctypes.c_uint64), ("end_cycles", ctypes.c_uint64)]
 
 
 class Group(ctypes.Structure):
@@ -106,6 +112,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         "gg_status_string": ([i32], ctypes.c_char_p),
         "gg_version": ([], i32),
         "gg_checked_build": ([], i32),
+        "gg_set_trace": ([i32], i32),
+        "gg_trace_read": ([vp, ctypes.POINTER(TraceRecord), ctypes.POINTER(TraceRecord)], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)

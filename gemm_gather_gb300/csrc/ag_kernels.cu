@@ -323,7 +323,7 @@ __device__ __forceinline__ void load_member_bases(const GatherArgs &a, uint64_t 
 // D: store groups a pipeline may leave reading shared memory before it
 // refills the oldest stage; the loads run stages - D items ahead.
 template <int D>
-__global__ void __launch_bounds__(kAgWarps * 32)
+__global__ void __launch_bounds__(kAgWarps * 32, 1)
     ag_bulk_kernel(const GatherArgs a, int stages, int stage_bytes)
 {
     const int npipe = blockDim.x >> 5;
@@ -331,6 +331,7 @@ __global__ void __launch_bounds__(kAgWarps * 32)
     AgShared &sh = *reinterpret_cast<AgShared *>(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    trace_mark(a.trace, 0);
     if (kChecked && !extents_ok(a)) {
         if (threadIdx.x == 0)
             bounds_fault(a.status);
@@ -461,12 +462,13 @@ __global__ void __launch_bounds__(kAgWarps * 32)
         }
     }
     ptx::bulk_wait_all();
+    trace_mark(a.trace, 1);
 }
 
 // Tensor-map path: same ring pipeline as ag_bulk_kernel; a tile is one box.
 // in_map views the sources as {N, M, heaps} (all-to-all: {N, M, W, heaps}).
 template <int D>
-__global__ void __launch_bounds__(kAgWarps * 32)
+__global__ void __launch_bounds__(kAgWarps * 32, 1)
     ag_tma_kernel(const __grid_constant__ CUtensorMap in_map, const __grid_constant__ OutMaps out,
                   const GatherArgs a, int stages, int stage_bytes)
 {
@@ -475,6 +477,7 @@ __global__ void __launch_bounds__(kAgWarps * 32)
     AgShared &sh = *reinterpret_cast<AgShared *>(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    trace_mark(a.trace, 0);
     if (kChecked && !extents_ok(a)) {
         if (threadIdx.x == 0)
             bounds_fault(a.status);
@@ -589,6 +592,7 @@ __global__ void __launch_bounds__(kAgWarps * 32)
         }
     }
     ptx::bulk_wait_all();
+    trace_mark(a.trace, 1);
 }
 
 template <int VB>
@@ -611,6 +615,7 @@ __global__ void __launch_bounds__(kVecThreads) ag_vec_kernel(const GatherArgs a)
     using V = typename VecType<VB>::T;
     __shared__ uint64_t dst[kMaxWorld];
     __shared__ uint64_t src[kMaxWorld];
+    trace_mark(a.trace, 0);
     if (kChecked && !extents_ok(a)) {
         if (threadIdx.x == 0)
             bounds_fault(a.status);
@@ -682,6 +687,7 @@ __global__ void __launch_bounds__(kVecThreads) ag_vec_kernel(const GatherArgs a)
             }
         }
     }
+    trace_mark(a.trace, 1);
 }
 
 }  // namespace

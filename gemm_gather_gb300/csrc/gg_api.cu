@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -193,6 +194,40 @@ gg_status library_status(int **out)
 gg_status resolve_status(int **status)
 {
     return *status ? GG_OK : library_status(status);
+}
+
+}  // namespace
+
+// The library's trace records (one per device, gg_set_trace): the all-gather
+// family's last traced launch in words 0..3, the fused call's in words 4..7.
+static __device__ unsigned long long g_trace[gg::kTraceWords];
+
+namespace {
+
+std::mutex g_trace_mu;
+void *g_trace_ptr[kMaxDevices];
+std::atomic<int> g_trace_on{0};
+
+gg_status trace_records(unsigned long long **out)
+{
+    void *p = nullptr;
+    gg_status st = device_symbol(&g_trace, g_trace_ptr, g_trace_mu,
+                                 "cudaGetSymbolAddress of the trace records", &p);
+    *out = static_cast<unsigned long long *>(p);
+    return st;
+}
+
+// The trace record a launch writes: NULL unless tracing is on.
+gg_status resolve_trace(unsigned long long **trace, int which)
+{
+    *trace = nullptr;
+    if (!g_trace_on.load(std::memory_order_relaxed))
+        return GG_OK;
+    unsigned long long *base = nullptr;
+    gg_status st = trace_records(&base);
+    if (st == GG_OK)
+        *trace = base + which;
+    return st;
 }
 
 }  // namespace
@@ -509,6 +544,8 @@ gg_status run_collective(const gg_heap *heap, int mode, int rank, const void *in
     if (st != GG_OK || !launch)
         return st;
     st = resolve_status(&a.status);
+    if (st == GG_OK)
+        st = resolve_trace(&a.trace, gg::kTraceGather);
     if (st != GG_OK)
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -791,6 +828,8 @@ gg_status gg_matmul_all_gather_path(const gg_heap *heap, int rank, const void *A
         return e == cudaSuccess ? ok() : cuda_fail(e, "launching the zero fill (K == 0)");
     }
     st = resolve_status(&f.status);
+    if (st == GG_OK)
+        st = resolve_trace(&f.trace, gg::kTraceFused);
     if (st != GG_OK)
         return st;
     const char *why = nullptr;
@@ -899,6 +938,33 @@ gg_status gg_clear_device_status(gg_stream_t stream)
     return ok();
 }
 
+gg_status gg_set_trace(int enable)
+{
+    g_trace_on.store(enable ? 1 : 0);
+    return ok();
+}
+
+gg_status gg_trace_read(gg_stream_t stream, gg_trace_record *gather, gg_trace_record *fused)
+{
+    static_assert(sizeof(gg_trace_record) == 4 * sizeof(unsigned long long), "record layout");
+    unsigned long long *rec = nullptr;
+    gg_status st = trace_records(&rec);
+    if (st != GG_OK)
+        return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    unsigned long long host[gg::kTraceWords];
+    cudaError_t e = cudaMemcpyAsync(host, rec, sizeof(host), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "reading the trace records");
+    if (gather)
+        memcpy(gather, host + gg::kTraceGather, sizeof(*gather));
+    if (fused)
+        memcpy(fused, host + gg::kTraceFused, sizeof(*fused));
+    return ok();
+}
+
 const char *gg_last_error(void) { return g_last_error.c_str(); }
 
 const char *gg_status_string(gg_status s)
@@ -982,6 +1048,8 @@ gg_status gg_all_gather_noalloc(const gg_heap *heap, int rank, const void *input
     if (st != GG_OK || !launch)
         return st;
     st = resolve_status(&a.status);
+    if (st == GG_OK)
+        st = resolve_trace(&a.trace, gg::kTraceGather);
     if (st != GG_OK)
         return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

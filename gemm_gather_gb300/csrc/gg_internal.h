@@ -10,6 +10,8 @@ namespace gg {
 constexpr int kMaxWorld = 64;
 constexpr int kStatusTimeout = -6;    // GG_ERR_TIMEOUT
 constexpr int kStatusNotInHeap = -3;  // GG_ERR_NOT_IN_HEAP (checked build)
+// Trace records (gg_set_trace): one per kernel family, 4 words each.
+constexpr int kTraceGather = 0, kTraceFused = 4, kTraceWords = 8;
 
 // Collectives the gather kernels run.
 constexpr int kModeGather = 0;       // every tile to every member
@@ -69,6 +71,7 @@ struct GatherArgs {
     unsigned long long *work;
     int chunk;         // items per claimed run
     int claim_policy;  // kClaimAuto / kClaimAlways / kClaimNever
+    unsigned long long *trace;  // non-null: the launch's trace record (see trace_mark)
 };
 
 constexpr int kClaimAuto = 0, kClaimAlways = 1, kClaimNever = 2;
@@ -107,6 +110,7 @@ struct FusedArgs {
     int b_boxes3d;     // set by the launcher: B stages load as one 3-d box
     int wide;          // 128 x 512 CTA tiles (256 x 512 per pair): two MMAs per A stage
     int tn_group;      // set by the launcher: tile columns per group of the tile order
+    unsigned long long *trace;  // non-null: the launch's trace record (see trace_mark)
 };
 
 // Fused kernel variants: 1 = 1-SM (one CTA per 128 x 256 tile), 2 = CTA

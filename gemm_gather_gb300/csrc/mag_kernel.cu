@@ -470,6 +470,7 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
                                          const OutMaps &out, const FusedArgs &a)
 {
     using G = Geo<CG>;
+    trace_mark(a.trace, 0);
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-aligned for the 128B swizzle
@@ -794,6 +795,7 @@ __device__ __forceinline__ void mag_body(const CUtensorMap &map_a, const CUtenso
         tc_fence_after();
         tmem_dealloc<CG>(tmem);
     }
+    trace_mark(a.trace, 1);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -916,6 +918,7 @@ __device__ __forceinline__ void magw_body(const CUtensorMap &map_a, const CUtens
 
     if (warp == 0) {
         // ===================== producer =====================================
+        trace_mark(a.trace, 0);
         const uint64_t pol_a = ptx::policy_evict_normal();
         const uint64_t pol_b = ptx::policy_evict_last();
         int stage = 0;
@@ -1161,6 +1164,7 @@ __device__ __forceinline__ void magw_body(const CUtensorMap &map_a, const CUtens
         tc_fence_after();
         tmem_dealloc<2>(tmem);
     }
+    trace_mark(a.trace, 1);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(wide::kThreads, 1)

@@ -179,4 +179,16 @@ __device__ __forceinline__ void report_status(int *status, int code)
         atomicCAS(status, 0, code);
 }
 
+// Trace record of a launch (gg_set_trace): the first CTA's wall time
+// (%globaltimer, ns) and SM cycle counter at its start (at_end = 0: words 0,
+// 1) and at its end (at_end = 1: words 2, 3).  Their ratio is the SM clock the
+// kernel ran at; one thread writes, once at each end.
+__device__ __forceinline__ void trace_mark(unsigned long long *trace, int at_end)
+{
+    if (trace != nullptr && blockIdx.x == 0 && threadIdx.x == 0) {
+        trace[2 * at_end] = ptx::globaltimer();
+        trace[2 * at_end + 1] = (unsigned long long)clock64();
+    }
+}
+
 }  // namespace gg

@@ -432,6 +432,35 @@ const char *gg_status_string(gg_status s);
 int gg_version(void);
 
 /* ---------------------------------------------------------------------------
+ * Tracing: the SM clock a kernel ran at.  The pages have no counterpart
+ * (their evidence is the compiler's assembly); here it shows how a kernel's
+ * time splits into SM cycles and clock.
+ *
+ * gg_set_trace(enable): launches after this call (enable != 0) record, from
+ * one thread of their first CTA, the wall time (%globaltimer, ns) and the SM
+ * cycle counter (clock64) at that CTA's start and end, into the library's
+ * trace records of the device: one record for the all-gather family (also
+ * gg_all_gather_noalloc), one for gg_matmul_all_gather.  enable == 0 (the
+ * default) stops it.  The cost is four 8-byte stores per launch.  The
+ * records are shared by every launch on the device, so with launches in
+ * flight on several streams the record is the last one written.
+ * (end_cycles - start_cycles) * 1e3 / (end_ns - start_ns) is the clock in
+ * MHz; the first CTA runs from a kernel's start to about its end.
+ *
+ * gg_trace_read(stream, gather, fused): copies the two records to the host
+ * after stream's queued work (either pointer may be NULL).  A record no
+ * traced launch has written holds zeros.  Like the status word, the records'
+ * address is looked up once per device and goes stale after a
+ * cudaDeviceReset of that device.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    uint64_t start_ns, start_cycles, end_ns, end_cycles;
+} gg_trace_record;
+
+gg_status gg_set_trace(int enable);
+gg_status gg_trace_read(gg_stream_t stream, gg_trace_record *gather, gg_trace_record *fused);
+
+/* ---------------------------------------------------------------------------
  * gg_checked_build — 1 in the checked build of the library
  * (libgemm_gather_checked.so), 0 in the release build (libgemm_gather.so).
  * The pages have no counterpart.
