@@ -4,9 +4,11 @@
  *
  * C ABI.  Plain pointers and sizes only.  All device memory is owned by the
  * caller; the library never allocates device memory, and its only device
- * state is two small static objects per device: the 256-byte counter array
- * of gg_all_gather_noalloc and the int status word of launches given no
- * status word (gg_device_status).  Every call that launches work is
+ * state is three small static objects per device: the 256-byte counter array
+ * of gg_all_gather_noalloc, the int status word of launches given no status
+ * word (gg_device_status) and 64 bytes of trace records (gg_set_trace).  The
+ * same calls also come in a checked build (gg_checked_build) with
+ * device-side bounds checks in the gather kernels.  Every call that launches work is
  * asynchronous on the caller's stream.  Errors found on the host are
  * returned before anything is launched; gg_last_error() then describes
  * them.  No call aborts the process.
