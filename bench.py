@@ -633,6 +633,8 @@ def run_sweep(args):
     import gg_inputs
     if args.claims is not None:
         gg.set_claim_policy(args.claims)
+    if args.store_policy is not None:
+        gg.set_store_policy(args.store_policy)
     peaks, peak_src = load_peaks()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
@@ -780,6 +782,9 @@ def main():
                     help="sweep: timed runs per point; the median is reported")
     ap.add_argument("--sweep-clocks", action="store_true",
                     help="sample SM clocks while each sweep point runs (about 1 s per point)")
+    ap.add_argument("--store-policy", default=None, choices=["plain", "evict_first"],
+                    help="L2 hint on the gather family's stores (default: the library's, "
+                    "evict_first)")
     ap.add_argument("--claims", default=None, choices=["auto", "always", "never"],
                     help="which gather launches claim runs of tiles from the heap's workspace "
                     "(default: the library's, auto)")
@@ -806,6 +811,8 @@ def main():
 
     if args.claims is not None:
         gg.set_claim_policy(args.claims)
+    if args.store_policy is not None:
+        gg.set_store_policy(args.store_policy)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))

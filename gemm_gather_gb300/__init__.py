@@ -29,7 +29,8 @@ __all__ = [
     "all_gather_check", "all_gather_grouped", "all_gather_partitioned", "all_to_all",
     "collective_check", "matmul_all_gather", "matmul_all_gather_check", "matmul_all_gather_plan",
     "set_claim_policy",
-    "get_claim_policy", "CLAIM_POLICIES", "set_wait_limit_ns",
+    "get_claim_policy", "CLAIM_POLICIES", "set_store_policy", "get_store_policy",
+    "STORE_POLICIES", "set_wait_limit_ns",
     "get_wait_limit_ns", "debug_inject_stall", "device_status", "clear_device_status",
     "checked_build", "set_trace", "trace_read", "SymmetricHeap", "Heap", "GGError", "DTYPE_CODES", "PATHS",
     "FUSED_TILE", "FUSED_TILE_WIDE", "FUSED_PATHS",
@@ -41,6 +42,7 @@ FUSED_PATHS = {"auto": GG_MAG_AUTO, "1sm": GG_MAG_1SM, "2sm": GG_MAG_2SM}
 FUSED_TILE = (GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N)             # 128 x 256 per CTA
 FUSED_TILE_WIDE = (GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N_WIDE)   # 128 x 512 per CTA (CTA pairs)
 CLAIM_POLICIES = {"auto": GG_CLAIM_AUTO, "always": GG_CLAIM_ALWAYS, "never": GG_CLAIM_NEVER}
+STORE_POLICIES = {"plain": 0, "evict_first": 1}  # GG_STORE_PLAIN, GG_STORE_EVICT_FIRST
 
 
 def _ptr(x) -> int | None:
@@ -249,6 +251,18 @@ def set_claim_policy(policy: str) -> None:
 def get_claim_policy() -> str:
     code = int(lib.gg_get_claim_policy())
     return next(k for k, v in CLAIM_POLICIES.items() if v == code)
+
+
+def set_store_policy(policy: str) -> None:
+    """L2 hint on the all-gather family's tensor-map and bulk stores:
+    "evict_first" (the library's default) or "plain" (none).  Results are
+    identical."""
+    check(lib.gg_set_store_policy(STORE_POLICIES[policy]))
+
+
+def get_store_policy() -> str:
+    code = int(lib.gg_get_store_policy())
+    return next(k for k, v in STORE_POLICIES.items() if v == code)
 
 
 def set_wait_limit_ns(ns: int) -> None:

@@ -34,6 +34,7 @@ GG_MAX_HEAPS = 1024
 GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N, GG_FUSED_BLOCK_N_WIDE = 128, 256, 512
 GG_WORKSPACE_SLOT_BYTES = 128
 GG_CLAIM_AUTO, GG_CLAIM_ALWAYS, GG_CLAIM_NEVER = 0, 1, 2
+GG_STORE_PLAIN, GG_STORE_EVICT_FIRST = 0, 1
 
 # Every entry point declared in include/gemm_gather.h.
 EXPORTS = (
@@ -44,7 +45,7 @@ EXPORTS = (
     "gg_all_gather_partitioned", "gg_all_to_all", "gg_collective_check",
     "gg_matmul_all_gather", "gg_matmul_all_gather_path", "gg_matmul_all_gather_check",
     "gg_matmul_all_gather_plan",
-    "gg_set_claim_policy", "gg_get_claim_policy",
+    "gg_set_claim_policy", "gg_get_claim_policy", "gg_set_store_policy", "gg_get_store_policy",
     "gg_set_wait_limit_ns", "gg_get_wait_limit_ns", "gg_debug_inject_stall",
     "gg_device_status", "gg_clear_device_status",
     "gg_set_trace", "gg_trace_read",
@@ -103,6 +104,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
                                        Tile, i32, Group, i32, ctypes.POINTER(i32)], i32),
         "gg_set_claim_policy": ([i32], i32),
         "gg_get_claim_policy": ([], i32),
+        "gg_set_store_policy": ([i32], i32),
+        "gg_get_store_policy": ([], i32),
         "gg_set_wait_limit_ns": ([u64], i32),
         "gg_get_wait_limit_ns": ([], u64),
         "gg_debug_inject_stall": ([i32], i32),

@@ -303,6 +303,17 @@ __device__ __forceinline__ void tma_store_box(const CUtensorMap *map, uint32_t s
         : "memory");
 }
 
+// The same store with an L2 eviction-priority hint (gg_set_store_policy).
+__device__ __forceinline__ void tma_store_box_hint(const CUtensorMap *map, uint32_t src, int c0,
+                                                   int c1, int c2, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+        " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
 // Heap bases -> per-member input and output bases, once per program.
 __device__ __forceinline__ void load_member_bases(const GatherArgs &a, uint64_t *dst,
                                                   uint64_t *src)
@@ -354,6 +365,7 @@ __global__ void __launch_bounds__(kAgWarps * 32, 1)
     const uint32_t ring = ptx::smem_addr(smem + kAgHeader) + (uint32_t)(warp * stages * stage_bytes);
     const uint32_t full0 = ptx::smem_addr(&sh.full[warp][0]);
     const uint32_t pitch = (uint32_t)a.bn_b;  // staged row pitch (multiple of 16)
+    const uint64_t pol_st = a.store_hint ? ptx::policy_evict_first() : 0;
     const int grp = (a.dests_per_wait > 0 && a.dests_per_wait < a.W) ? a.dests_per_wait : a.W;
 
     // Takes the pipeline's next item (if any) and starts its load into ring
@@ -441,7 +453,10 @@ __global__ void __launch_bounds__(kAgWarps * 32, 1)
                     bounds_fault(a.status);
                     continue;
                 }
-                ptx::bulk_s2g(dst, buf + (uint32_t)r * pitch, it.rb);
+                if (a.store_hint)
+                    ptx::bulk_s2g_hint(dst, buf + (uint32_t)r * pitch, it.rb, pol_st);
+                else
+                    ptx::bulk_s2g(dst, buf + (uint32_t)r * pitch, it.rb);
             }
             ptx::bulk_commit();
             if (j0 + grp < a.W) {  // the next group waits until this one has read its data
@@ -503,6 +518,7 @@ __global__ void __launch_bounds__(kAgWarps * 32, 1)
     const uint32_t ring = ptx::smem_addr(smem + kAgHeader) + (uint32_t)(warp * stages * stage_bytes);
     const uint32_t full0 = ptx::smem_addr(&sh.full[warp][0]);
     const uint32_t box_bytes = (uint32_t)(a.bm * a.bn_b);  // a full box, clipped parts zero-filled
+    const uint64_t pol_st = a.store_hint ? ptx::policy_evict_first() : 0;
     const int bn = (int)(a.bn_b / a.es);
     const int grp = (a.dests_per_wait > 0 && a.dests_per_wait < a.W) ? a.dests_per_wait : a.W;
 
@@ -565,7 +581,10 @@ __global__ void __launch_bounds__(kAgWarps * 32, 1)
                     int i = it.g + j;
                     if (i >= a.W)
                         i -= a.W;
-                    tma_store_box(&out.map[i], buf, c0, c1, it.g);
+                    if (a.store_hint)
+                        tma_store_box_hint(&out.map[i], buf, c0, c1, it.g, pol_st);
+                    else
+                        tma_store_box(&out.map[i], buf, c0, c1, it.g);
                 }
                 ptx::bulk_commit();
                 if (jend < a.W) {
@@ -575,9 +594,13 @@ __global__ void __launch_bounds__(kAgWarps * 32, 1)
             }
         } else {
             // one destination: the program's own (partitioned) or the block's (all-to-all)
-            if (lane == 0)
-                tma_store_box(&out.map[a.mode == kModePartitioned ? dest : it.d], buf, c0, c1,
-                              it.g);
+            if (lane == 0) {
+                const CUtensorMap *m = &out.map[a.mode == kModePartitioned ? dest : it.d];
+                if (a.store_hint)
+                    tma_store_box_hint(m, buf, c0, c1, it.g, pol_st);
+                else
+                    tma_store_box(m, buf, c0, c1, it.g);
+            }
             ptx::bulk_commit();
         }
         __syncwarp();

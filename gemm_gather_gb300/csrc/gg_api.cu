@@ -44,6 +44,7 @@ thread_local std::string g_last_error;
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_claim_policy{GG_CLAIM_AUTO};
+std::atomic<int> g_store_policy{GG_STORE_EVICT_FIRST};
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 
 gg_status fail(gg_status s, const char *fmt, ...)
@@ -454,6 +455,8 @@ gg_status prepare_gather(const gg_heap *heap, int mode, int rank, const void *in
     a.work = nullptr;  // a slot is taken at launch time
     a.chunk = 0;
     a.claim_policy = g_claim_policy.load();
+    a.store_hint = g_store_policy.load() == GG_STORE_EVICT_FIRST ? gg::kStoreEvictFirst
+                                                                 : gg::kStorePlain;
 
     // widest power-of-two granule dividing every address, pitch and length
     uint64_t g = in_align | (uint64_t)out_off | (uint64_t)a.ld_in_b | (uint64_t)a.ld_out_b |
@@ -902,6 +905,16 @@ gg_status gg_set_claim_policy(int policy)
 }
 
 int gg_get_claim_policy(void) { return g_claim_policy.load(); }
+
+gg_status gg_set_store_policy(int policy)
+{
+    if (policy != GG_STORE_PLAIN && policy != GG_STORE_EVICT_FIRST)
+        return fail(GG_ERR_INVALID_ARG, "unknown store policy %d", policy);
+    g_store_policy.store(policy);
+    return ok();
+}
+
+int gg_get_store_policy(void) { return g_store_policy.load(); }
 
 gg_status gg_debug_inject_stall(int enable)
 {

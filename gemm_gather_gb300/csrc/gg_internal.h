@@ -72,9 +72,11 @@ struct GatherArgs {
     int chunk;         // items per claimed run
     int claim_policy;  // kClaimAuto / kClaimAlways / kClaimNever
     unsigned long long *trace;  // non-null: the launch's trace record (see trace_mark)
+    int store_hint;             // kStorePlain / kStoreEvictFirst (tensor-map and bulk stores)
 };
 
 constexpr int kClaimAuto = 0, kClaimAlways = 1, kClaimNever = 2;
+constexpr int kStorePlain = 0, kStoreEvictFirst = 1;
 // Bytes of one workspace slot (a counter, padded to its own 128 bytes).
 constexpr int kWorkSlotBytes = 128;
 

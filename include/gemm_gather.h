@@ -153,6 +153,25 @@ gg_status gg_set_claim_policy(int policy);
 int gg_get_claim_policy(void);
 
 /* ---------------------------------------------------------------------------
+ * gg_set_store_policy — an L2 eviction-priority hint on the stores of the
+ * all-gather family (the pages' store-policy knob: the Gluon all-gather's
+ * local copy stores with a write-through cache policy, iris #594 "PR
+ * description").  GG_STORE_EVICT_FIRST (the default): every TMA tensor
+ * store (tensor-map path) and bulk store (bulk path) carries an L2
+ * evict_first hint, so the gathered output, written once and not read again
+ * by the launch, is the first to leave L2 (measured on GB300: 0.25% faster
+ * than plain stores at W=8 16384x8192 f32 and 4096x4096 f16).
+ * GG_STORE_PLAIN: no hint.  The vector path stores without a hint.  Results
+ * are identical either way.
+ * Process-wide (all devices and threads), read when a call is validated.
+ * Anything else returns GG_ERR_INVALID_ARG.
+ * ------------------------------------------------------------------------- */
+#define GG_STORE_PLAIN 0
+#define GG_STORE_EVICT_FIRST 1
+gg_status gg_set_store_policy(int policy);
+int gg_get_store_policy(void);
+
+/* ---------------------------------------------------------------------------
  * gg_all_gather — the persistent tiled all-gather (iris PR #626, "Triton CCL
  * all-gather"; iris #594, "PR description"; iris #591, Description §1).
  *

@@ -342,3 +342,16 @@ def test_binding_stream_argument():
     assert _stream(0) is None
     if not torch.cuda.is_initialized():
         assert _stream(None) is None
+
+
+def test_store_policy_round_trip():
+    assert gg.get_store_policy() == "evict_first"  # the library's default
+    try:
+        gg.set_store_policy("plain")
+        assert gg.get_store_policy() == "plain"
+        with pytest.raises(gg.GGError) as e:
+            gg.check(gg.lib.gg_set_store_policy(7))
+        assert e.value.status == _lib.GG_ERR_INVALID_ARG
+        assert gg.get_store_policy() == "plain"
+    finally:
+        gg.set_store_policy("evict_first")

@@ -174,3 +174,37 @@ def test_binding_uses_torch_current_stream():
     with torch.cuda.stream(s):
         assert _stream(None) == s.cuda_stream
     assert _stream(s) == s.cuda_stream
+
+
+@pytest.fixture
+def plain_stores():
+    """Every other test runs with the library's default hint (evict_first);
+    these run the plain stores."""
+    import gemm_gather_gb300 as gg
+    gg.set_store_policy("plain")
+    yield
+    gg.set_store_policy("evict_first")
+
+
+@pytest.mark.parametrize("path", ["tma", "bulk", "vector"])
+@pytest.mark.parametrize("mode", ["group", "ranks"])
+def test_store_policy_plain_changes_no_byte(oracle, plain_stores, path, mode):
+    """Plain stores (no L2 hint, gg_set_store_policy) leave the whole heap
+    exactly as the oracle's: ragged tiles, padded pitches, a strided subgroup
+    with inactive heaps."""
+    _run_case(oracle, 8, (1, 2, 3), 72, 520, 2, (16, 128), 7, pad_in=8, pad_out=24, path=path,
+              mode=mode)
+    _run_case(oracle, 4, (0, 1, 4), 256, 1024, 4, (8, 256), 148, path=path, mode=mode, seed=2)
+
+
+def test_store_policy_collectives(oracle, plain_stores):
+    """The partitioned all-gather, the grouped all-gather and the all-to-all
+    with plain stores: the result is unchanged."""
+    from tests.test_gpu_collectives import (PART_CASES, test_all_to_all_matches_oracle,
+                                            test_grouped_all_gather_matches_oracle,
+                                            test_partitioned_all_gather_matches_oracle)
+    test_partitioned_all_gather_matches_oracle(oracle, PART_CASES[3], "tma")
+    test_grouped_all_gather_matches_oracle(oracle, 3, "tma")
+    test_grouped_all_gather_matches_oracle(oracle, 2, "bulk")
+    from tests.test_gpu_collectives import A2A_CASES
+    test_all_to_all_matches_oracle(oracle, A2A_CASES[3], "tma", "group")
