@@ -690,7 +690,7 @@ gg_status prepare_fused(const gg_heap *heap, int rank, const void *A, int64_t ld
     if (tile.block_m != GG_FUSED_BLOCK_M ||
         (tile.block_n != GG_FUSED_BLOCK_N && tile.block_n != GG_FUSED_BLOCK_N_WIDE))
         return fail(GG_ERR_UNSUPPORTED,
-                    "fused tile %dx%d is not supported; this build runs %dx%d and %dx%d (tiles are "
+                    "fused tile %dx%d is not supported; the library runs %dx%d and %dx%d (tiles are "
                     "never remapped)",
                     tile.block_m, tile.block_n, GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N,
                     GG_FUSED_BLOCK_M, GG_FUSED_BLOCK_N_WIDE);

@@ -51,7 +51,7 @@ typedef enum {
     GG_ERR_ALIGNMENT = -2,    /* pointer/pitch alignment a path requires     */
     GG_ERR_NOT_IN_HEAP = -3,  /* a symmetric buffer does not fit a partition;
                                  checked build: a device access out of bounds */
-    GG_ERR_UNSUPPORTED = -4,  /* valid request this build does not implement */
+    GG_ERR_UNSUPPORTED = -4,  /* valid request the library does not implement */
     GG_ERR_CUDA = -5,         /* a CUDA runtime call failed                  */
     GG_ERR_TIMEOUT = -6       /* device: a bounded wait gave up (status word)*/
 } gg_status;
