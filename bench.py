@@ -683,7 +683,10 @@ def run_sweep(args):
                 runs.append(e0.elapsed_time(e1) / steps)
             return runs, steps, (clocks.stop() if clocks else None)
 
+        gg.set_trace(True)  # the kernel's own SM clock, from its last timed launch
         runs, steps, clk = timed(launch)
+        trace = gg.trace_read()
+        gg.set_trace(False)
         ms = statistics.median(runs)
         if int(status.item()) != 0:
             raise RuntimeError(f"device status {int(status.item())}")
@@ -726,6 +729,13 @@ def run_sweep(args):
             torch.cuda.synchronize(dev)
             rec["us_per_launch"] = 1e3 * ms
             rec["graph_us_per_launch"] = g0.elapsed_time(g1) / 1000 * 1e3
+        kclk = kernel_clock(trace["all_gather" if g else "matmul_all_gather"])
+        if kclk:
+            if f:
+                sms = torch.cuda.get_device_properties(dev).multi_processor_count
+                kclk["per_clock_frac"] = fused_flops(f) / (kclk["cycles"] * sms *
+                                                           TC_FLOP_PER_SM_CYCLE)
+            rec["kernel_clock"] = kclk
         if clk:
             rec["clocks"] = clk
             if f:
