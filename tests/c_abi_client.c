@@ -13,6 +13,8 @@
  *     and |C| <= 256 is exact in binary16, so each output element must equal
  *     the integer dot product computed here.
  *   status: a launch given no status word leaves the library's word at 0.
+ *   the gather runs with plain stores (gg_set_store_policy) and traced
+ *   (gg_set_trace): its trace record must show time and cycles passing.
  *
  * Prints "c abi client ok" and returns 0 on success; any mismatch or error
  * prints what failed and returns 1.
@@ -90,9 +92,24 @@ static int run_gather(void)
     CHECK_GG(gg_heap_create(heap_mem, part, W, table, NULL, &heap));
     gg_tile tile = {8, 256};
     gg_group group = {0, 1, W};
+    /* plain stores (no L2 hint) and a traced launch */
+    CHECK_GG(gg_set_store_policy(GG_STORE_PLAIN));
+    if (gg_get_store_policy() != GG_STORE_PLAIN || gg_set_store_policy(5) != GG_ERR_INVALID_ARG) {
+        fprintf(stderr, "store policy round trip\n");
+        return 1;
+    }
+    CHECK_GG(gg_set_trace(1));
     CHECK_GG(gg_all_gather(heap, -1, (char *)heap_mem + in_off, N, (char *)heap_mem + out_off,
                            LD_OUT, M, N, GG_F16, tile, 16, group, (int *)status, NULL));
     CHECK_CUDA(cudaDeviceSynchronize());
+    gg_trace_record rec;
+    CHECK_GG(gg_trace_read(NULL, &rec, NULL));
+    CHECK_GG(gg_set_trace(0));
+    CHECK_GG(gg_set_store_policy(GG_STORE_EVICT_FIRST));
+    if (!(rec.end_ns > rec.start_ns && rec.end_cycles > rec.start_cycles)) {
+        fprintf(stderr, "trace record not written\n");
+        return 1;
+    }
     int st = -1;
     CHECK_CUDA(cudaMemcpy(&st, status, sizeof(int), cudaMemcpyDeviceToHost));
     if (st != 0) {
