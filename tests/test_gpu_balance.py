@@ -189,9 +189,10 @@ def test_concurrent_launches_on_several_streams(oracle):
     """Five launches in flight at once on five streams, into disjoint output
     regions of one heap: two claiming tensor-map all-gathers (each takes its
     own workspace slot), a grouped bulk all-gather, a partitioned all-gather on
-    the vector path and a claiming all-to-all.  Each region must hold the
-    oracle's result and nothing else may change, as if the launches had run
-    one after another; every status word stays 0."""
+    the vector path and a claiming all-to-all; plus a fused matmul +
+    all-gather on a sixth stream into a second heap.  Each region must hold
+    the oracle's result and nothing else may change, as if the launches had
+    run one after another; every status word stays 0."""
     import gemm_gather_gb300 as gg
     H, group, M, N, es, tile = 4, (0, 1, 4), 256, 2048, 2, (8, 256)
     W = group[2]
@@ -223,10 +224,33 @@ def test_concurrent_launches_on_several_streams(oracle):
         lambda s, st: gg.all_to_all(sh.heap, -1, inp, N, sh.ptr(0, out[4]), N, M, N, DT[es],
                                     tile, 3, group, status=st, stream=s, path="tma"),
     ]
+    # and a fused matmul + all-gather (integer operands: exact) on a sixth stream,
+    # into a heap of its own
+    fW, fM, fN, fK = 2, 256, 512, 128
+    fl = hi.make_layout(fW, fW, fM, fN, 2, ld_in=fK)
+    fhost = hi.sentinel_heap(fl)
+    fgen = gg_inputs.generator(5)
+    for h in range(fW):
+        a = gg_inputs.integers((fM, fK), -2, 2, torch.float16, fgen)
+        hi.put_block(fhost, fl, h, a.view(torch.int16).numpy().view(np.uint16), fl.in_off, fK)
+    fB = gg_inputs.integers((fK, fN), -2, 2, torch.float16, fgen)
+    fh = device_heap(fl, fhost)
+    fB_dev = fB.to("cuda")
+    fstatus = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    fstream = torch.cuda.Stream()
     for s, call, st in zip(streams, calls, status):
         call(s, st)
+    gg.matmul_all_gather(fh.heap, -1, fh.ptr(0, fl.in_off), fK, fB_dev, fN, fh.ptr(0, fl.out_off),
+                         fN, fM, fN, fK, torch.float16, gg.FUSED_TILE_WIDE, 8, (0, 1, fW),
+                         status=fstatus, stream=fstream)
     got = download(sh)
-    assert status.tolist() == [0] * 5
+    fgot = download(fh)
+    assert status.tolist() == [0] * 5 and int(fstatus.item()) == 0
+    oracle.matmul_all_gather(fhost, fl.part_bytes, fl.in_off, fK,
+                             fB.view(torch.int16).numpy().view(np.uint16), fl.out_off, fN, fM, fN,
+                             fK, 0, (0, 1, fW))
+    assert np.array_equal(fgot, fhost), first_diff(fgot, fhost, fl)
     for j in range(4):
         oracle.all_gather(host, part, lay.in_off, N, out[j], N, M, N, es, group)
     oracle.all_to_all(host, part, lay.in_off, N, out[4], N, M, N, es, group)
